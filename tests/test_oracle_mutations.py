@@ -1,0 +1,60 @@
+"""Planted mistakes: each plausible slip in the oracle (a dropped term, a wrong
+sign or index, a transposed operand) must make at least one pin fail.
+
+The mistakes are planted in a private copy of the oracle's source, on the CPU;
+the oracle itself is never modified."""
+import importlib.util
+import os
+import sys
+import types
+
+import pytest
+
+from oracle_pins import ALL_PINS
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                   "oracle", "attention.py")
+
+MUTATIONS = {
+    "dropped_scale": ("s = scale * (qrows @ k[keys].T)", "s = (qrows @ k[keys].T)"),
+    "alibi_sign": ("s = s - slope * dist", "s = s + slope * dist"),
+    "diagonal_masked": ("keys[None, :] <= rows[:, None]", "keys[None, :] < rows[:, None]"),
+    "zigzag_pairing": ("shards[r].extend(chunks[2 * N - 1 - r])", "shards[r].extend(chunks[N + r])"),
+    "zigzag_order": ("shards[r].extend(chunks[r])\n            shards[r].extend(chunks[2 * N - 1 - r])",
+                     "shards[r].extend(chunks[2 * N - 1 - r])\n            shards[r].extend(chunks[r])"),
+    "q_k_swapped": ("s = _scores(q[b, h, r], k[b, h], r, keys, scale, slope, causal)\n                lse = _row_lse(s)",
+                    "s = _scores(k[b, h, r], q[b, h], r, keys, scale, slope, causal)\n                lse = _row_lse(s)"),
+    "lse_no_log": ("lse = safe + np.log(tot)", "lse = safe + tot"),
+    "ds_missing_D": ("ds = p * (dp - Dvec[r][:, None])", "ds = p * dp"),
+    "dk_unscaled": ("dk[b, h] += scale * (ds.T @ q[b, h, r])\n    return dq, dk, dv",
+                    "dk[b, h] += (ds.T @ q[b, h, r])\n    return dq, dk, dv"),
+    "dv_wrong_operand": ("dv[b, h] += p.T @ dout[b, h, r]\n                dq[b, h, r]",
+                         "dv[b, h] += p.T @ v[b, h, r]\n                dq[b, h, r]"),
+    "merge_max": ("lse = np.logaddexp(lse_a, lse_b)", "lse = np.maximum(lse_a, lse_b)"),
+    "online_alpha_inverted": ("alpha = np.where(np.isfinite(m), np.exp(m - ref), 0.0)",
+                              "alpha = np.where(np.isfinite(m), np.exp(ref - m), 0.0)"),
+    "ring_direction_skips": ("steps = [(r - t) % N for t in range(N)]", "steps = [(r - t) % N for t in range(1, N)]"),
+    "pairs_off_by_one": ("int(sum(g + 1 for g in shard))", "int(sum(g for g in shard))"),
+}
+
+
+def _load_mutant(name, old, new):
+    with open(SRC) as f:
+        text = f.read()
+    assert text.count(old) == 1, f"mutation {name}: anchor not found exactly once"
+    mod = types.ModuleType(f"oracle_mutant_{name}")
+    exec(compile(text.replace(old, new), f"<mutant {name}>", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(name):
+    old, new = MUTATIONS[name]
+    mod = _load_mutant(name, old, new)
+    caught = []
+    for pin in ALL_PINS:
+        try:
+            pin(mod)
+        except Exception as e:  # an assertion or a crash both count as caught
+            caught.append(pin.__name__)
+    assert caught, f"planted mistake {name!r} passed every pin"
