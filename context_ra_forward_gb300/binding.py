@@ -1,0 +1,181 @@
+"""Thin ctypes binding over the C ABI of include/ra.h.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of libra.so.  PyTorch supplies device memory and the current stream.
+If the library is not built (or fails to load) every call raises; there is no
+fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libra.so")
+
+RA_OK = 0
+STATUS_NAMES = {0: "RA_OK", -1: "RA_ERR_INVALID_ARG", -2: "RA_ERR_UNSUPPORTED",
+                -3: "RA_ERR_MISALIGNED", -4: "RA_ERR_CUDA", -5: "RA_ERR_TIMEOUT",
+                -6: "RA_ERR_WORKSPACE"}
+DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+LAYOUTS = {"contiguous": 0, "zigzag": 1}
+
+
+class RAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what} failed: {STATUS_NAMES.get(status, status)}")
+
+
+_lib = None
+
+_i64, _i32, _vp, _f32 = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_float
+
+
+def lib() -> ctypes.CDLL:
+    """Load libra.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is not built: run context_ra_forward_gb300.build.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    perm = [_vp, _vp, _i64, _i64, _i64, _i64, _i32, _i32, _i32, _vp]
+    L.ra_index_map.argtypes = [_i64, _i32, _i32, _vp, _vp]
+    L.ra_zigzag_permute.argtypes = perm
+    L.ra_unpermute.argtypes = perm
+    L.ra_forward.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32, _i32, _vp,
+                             _f32, _i32, _i32, _vp]
+    L.ra_backward_workspace_bytes.argtypes = [_i64, _i64, _i64, _i64]
+    L.ra_backward_workspace_bytes.restype = ctypes.c_size_t
+    L.ra_backward.argtypes = [_vp] * 10 + [ctypes.c_size_t, _i64, _i64, _i64, _i64, _i32, _i32,
+                                           _vp, _f32, _i32, _i32, _vp]
+    L.ra_status_string.argtypes = [_i32]
+    L.ra_status_string.restype = ctypes.c_char_p
+    L.ra_check_device_status.argtypes = [_vp, _vp]
+    L.ra_forward_path.argtypes = [_i64, _i64, _i64, _i64, _i32, _i32, _i32]
+    L.ra_debug_wait_timeout.argtypes = [_i32, _vp]
+    for name in ("ra_index_map", "ra_zigzag_permute", "ra_unpermute", "ra_forward", "ra_backward",
+                 "ra_check_device_status", "ra_forward_path", "ra_debug_wait_timeout"):
+        getattr(L, name).restype = ctypes.c_int32
+    _lib = L
+    return L
+
+
+def _check(status: int, what: str) -> None:
+    if status != RA_OK:
+        raise RAError(status, what)
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _bhsd(t: torch.Tensor, name: str):
+    if t.dim() != 4:
+        raise ValueError(f"{name} must be [B, H, S, D]")
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if t.dtype not in DTYPES:
+        raise ValueError(f"{name}: dtype {t.dtype} not supported (float32 or bfloat16)")
+    return t.shape
+
+
+def _layout(layout: str) -> int:
+    if layout not in LAYOUTS:
+        raise ValueError(f"layout must be one of {sorted(LAYOUTS)}")
+    return LAYOUTS[layout]
+
+
+def index_map(S: int, N: int, layout: str):
+    """(perm, inv) as int64 numpy arrays: perm[slot] = global position, inv = its inverse."""
+    perm = np.empty(S, dtype=np.int64)
+    inv = np.empty(S, dtype=np.int64)
+    _check(lib().ra_index_map(S, N, _layout(layout), perm.ctypes.data, inv.ctypes.data), "ra_index_map")
+    return perm, inv
+
+
+def _permute(fn, x, N, layout, out, stream):
+    B, H, S, D = _bhsd(x, "x")
+    y = torch.empty_like(x) if out is None else out
+    _bhsd(y, "out")
+    _check(fn(_ptr(x), _ptr(y), B, H, S, D, DTYPES[x.dtype], N, _layout(layout), _stream(stream)),
+           fn.__name__)
+    return y
+
+
+def zigzag_permute(x, N: int, layout: str = "zigzag", out=None, stream=None):
+    """Original order -> shard-major order (ra_zigzag_permute)."""
+    return _permute(lib().ra_zigzag_permute, x, N, layout, out, stream)
+
+
+def unpermute(x, N: int, layout: str = "zigzag", out=None, stream=None):
+    """Shard-major order -> original order (ra_unpermute)."""
+    return _permute(lib().ra_unpermute, x, N, layout, out, stream)
+
+
+def forward_path(B, H, S, D, dtype, N, layout) -> int:
+    """1 = tensor-core kernel, 2 = CUDA-core fp32 kernel, 0 = empty, < 0 = rejected."""
+    return lib().ra_forward_path(B, H, S, D, DTYPES[dtype], N, _layout(layout))
+
+
+def forward(q, k, v, *, causal=False, alibi_slopes=None, softmax_scale=None, N=1,
+            layout="contiguous", out=None, lse=None, stream=None):
+    """Exact attention over N virtual ring shards (ra_forward).  q/k/v are
+    [B, H, S, D] in shard-major order; returns (o, lse) in the same order."""
+    B, H, S, D = _bhsd(q, "q")
+    for t, n in ((k, "k"), (v, "v")):
+        if _bhsd(t, n) != q.shape or t.dtype != q.dtype:
+            raise ValueError(f"{n} must match q in shape and dtype")
+    o = torch.empty_like(q) if out is None else out
+    lse_t = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if lse is None else lse
+    if alibi_slopes is not None:
+        if alibi_slopes.dtype != torch.float32 or not alibi_slopes.is_cuda or alibi_slopes.numel() != H:
+            raise ValueError("alibi_slopes must be a float32 CUDA tensor of H elements")
+    scale = 0.0 if softmax_scale is None else float(softmax_scale)
+    _check(lib().ra_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse_t), B, H, S, D,
+                            DTYPES[q.dtype], int(bool(causal)), _ptr(alibi_slopes), scale, N,
+                            _layout(layout), _stream(stream)), "ra_forward")
+    return o, lse_t
+
+
+def backward_workspace_bytes(B, H, S, D) -> int:
+    return int(lib().ra_backward_workspace_bytes(B, H, S, D))
+
+
+def backward(q, k, v, o, lse, dout, *, causal=False, alibi_slopes=None, softmax_scale=None,
+             N=1, layout="contiguous", workspace=None, out=None, stream=None):
+    """dQ, dK, dV (ra_backward), recomputing probabilities from the saved LSE."""
+    B, H, S, D = _bhsd(q, "q")
+    for t, n in ((k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
+        if _bhsd(t, n) != q.shape or t.dtype != q.dtype:
+            raise ValueError(f"{n} must match q in shape and dtype")
+    need = backward_workspace_bytes(B, H, S, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    dq, dk, dv = out if out is not None else (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    scale = 0.0 if softmax_scale is None else float(softmax_scale)
+    _check(lib().ra_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                             _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(), B, H, S, D,
+                             DTYPES[q.dtype], int(bool(causal)), _ptr(alibi_slopes), scale, N,
+                             _layout(layout), _stream(stream)), "ra_backward")
+    return dq, dk, dv
+
+
+def check_device_status(stream=None):
+    """Synchronise and read/clear the device status word: (status, [code, kernel, block, site])."""
+    detail = (ctypes.c_int32 * 4)()
+    st = lib().ra_check_device_status(_stream(stream), ctypes.cast(detail, ctypes.c_void_p))
+    return st, list(detail)
+
+
+def debug_wait_timeout(limit_us: int, stream=None) -> None:
+    _check(lib().ra_debug_wait_timeout(limit_us, _stream(stream)), "ra_debug_wait_timeout")

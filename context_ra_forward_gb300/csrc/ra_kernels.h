@@ -1,0 +1,48 @@
+// ra_kernels.h — launchers shared between the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ra_common.cuh"
+
+namespace ra {
+
+struct AttnArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  int64_t B, H, S, D;
+  int32_t dtype;
+  int32_t causal;
+  const float* slopes;  // device [H] or nullptr
+  float scale;          // resolved softmax scale (> 0)
+  SeqMap map;
+  int32_t* status;      // device status word
+};
+
+// ra_permute.cu
+cudaError_t launch_permute(const void* x, void* y, int64_t BH, int64_t S, int64_t row_bytes,
+                           const SeqMap& m, bool inverse, cudaStream_t st);
+
+// ra_simt.cu — CUDA-core kernels (exact fp32 arithmetic)
+cudaError_t launch_fwd_simt(const AttnArgs& a, void* o, float* lse, cudaStream_t st);
+cudaError_t launch_bwd_rowdot(const AttnArgs& a, const void* o, const void* dout, float* dvec,
+                              cudaStream_t st);
+cudaError_t launch_bwd_simt(const AttnArgs& a, const float* lse, const void* dout,
+                            const float* dvec, void* dq, void* dk, void* dv, cudaStream_t st);
+
+// ra_fwd_tc.cu — tcgen05 tensor-core forward (bf16, D = 128)
+bool fwd_tc_supported(int64_t S, int64_t D, int32_t dtype);
+cudaError_t launch_fwd_tc(const AttnArgs& a, void* o, float* lse, cudaStream_t st);
+
+// ra_bwd_tc.cu — tcgen05 tensor-core backward (bf16, D = 128)
+bool bwd_tc_supported(int64_t S, int64_t D, int32_t dtype);
+cudaError_t launch_bwd_tc(const AttnArgs& a, const float* lse, const void* dout,
+                          const float* dvec, float* dq_acc, void* dq, void* dk, void* dv,
+                          cudaStream_t st);
+
+// ra_debug.cu
+cudaError_t launch_debug_wait(int32_t limit_us, int32_t* status, cudaStream_t st);
+
+}  // namespace ra

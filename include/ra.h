@@ -1,0 +1,182 @@
+/*
+ * ra.h — ring / zig-zag blockwise exact attention on one GPU (sm_103a): C ABI.
+ *
+ * Pages cited (titles as printed):
+ *   [CP] "百万Token上下文训练的挑战与突破" — §2.1 序列切分策略对比 (split the
+ *        sequence into N equal pieces along the sequence dimension), §3.1 环形通信拓扑
+ *        (device i receives the K/V of device i-1, combines, passes on).
+ *   [ZZ] "大模型如何訓練百萬 Token 上下文：上下文并行與 Ring Attention" — §Zig Zag Ring
+ *        Attention (every shard's Q meets every K/V block, one ring step at a time;
+ *        interleaved assignment balances causal work; indexing is more involved).
+ *   [LC] "超长上下文技术" survey (intelliparadigm.com 2061774) — §2.1.2 ALiBi (scores
+ *        scaled by 1/sqrt(head dim), bias -|i-j|*slope added), §3.1.2 FlashAttention
+ *        (blockwise evaluation with a running max and sum; recompute in backward).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Tensors are [B, H, S, D] (batch, heads, sequence, head dim), contiguous, D
+ *    innermost.  Q/K/V/O/dO/dQ/dK/dV of one call share one dtype: RA_F32 (fp32) or
+ *    RA_BF16 (bf16).  LSE is always fp32 [B, H, S].  D must be 64 or 128.
+ *  - Sequence order.  Attention calls take and return tensors in SHARD-MAJOR order:
+ *    the N shards' token sequences concatenated, shard 0 first, which is what
+ *    ra_zigzag_permute produces.  Global token positions (for the causal mask and
+ *    ALiBi) are recovered from the slot index by the layout's closed form.
+ *  - Layouts.  RA_LAYOUT_CONTIGUOUS: shard r holds tokens [r*S/N, (r+1)*S/N)
+ *    ([CP] §2.1), needs S % N == 0.  RA_LAYOUT_ZIGZAG: the sequence is cut into 2N
+ *    chunks of h = S/(2N) tokens; shard r holds chunk r followed by chunk 2N-1-r
+ *    ([ZZ] §Zig Zag, 2N-chunk form), needs S % (2N) == 0.
+ *  - Pointers named "device" are CUDA device pointers (e.g. from PyTorch) and must
+ *    be 16-byte aligned (LSE and the slopes: 4-byte aligned).  The caller owns every
+ *    buffer; the library allocates no memory at call time and keeps no per-call
+ *    state.  (A device status word, created when the library is loaded, records
+ *    the first bounded-wait timeout a kernel hits; see ra_check_device_status.)
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  All compute
+ *    calls are asynchronous on it; arguments are validated on the host before any
+ *    launch and a failed validation launches nothing.  No C++ exception crosses
+ *    this interface.
+ *  - Zero-size problems (B, H or S == 0) validate their scalar arguments and
+ *    return RA_OK without launching.
+ */
+#ifndef RA_H_
+#define RA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t ra_status;
+#define RA_OK                 0
+#define RA_ERR_INVALID_ARG   -1  /* NULL pointer, bad size, S not divisible, N < 1, aliasing */
+#define RA_ERR_UNSUPPORTED   -2  /* D not 64/128, unknown dtype/layout, not an sm_103 device */
+#define RA_ERR_MISALIGNED    -3  /* a pointer not aligned as stated above */
+#define RA_ERR_CUDA          -4  /* a CUDA runtime/driver call or launch failed */
+#define RA_ERR_TIMEOUT       -5  /* a bounded in-kernel wait expired (ra_check_device_status) */
+#define RA_ERR_WORKSPACE     -6  /* backward workspace missing or too small */
+
+typedef int32_t ra_dtype;
+#define RA_F32   0
+#define RA_BF16  1
+
+typedef int32_t ra_layout;
+#define RA_LAYOUT_CONTIGUOUS 0
+#define RA_LAYOUT_ZIGZAG     1
+
+/*
+ * ra_index_map — the sequence -> shard assignment as explicit tables (host only).
+ * [CP] §2.1 (contiguous), [ZZ] §Zig Zag (2N-chunk interleave).
+ *   perm_host[p] = global token position held at shard-major slot p;
+ *   inv_host[g]  = shard-major slot of global position g.
+ * Both are caller-owned host arrays of S int64 (either may be NULL to skip it).
+ * Errors: RA_ERR_INVALID_ARG (S < 0, N < 1, S not divisible), RA_ERR_UNSUPPORTED
+ * (unknown layout).
+ */
+ra_status ra_index_map(int64_t S, int32_t N, ra_layout layout,
+                       int64_t* perm_host, int64_t* inv_host);
+
+/*
+ * ra_zigzag_permute — y[b,h,p,:] = x[b,h,perm(p),:]: original order -> shard-major.
+ * [ZZ] §Zig Zag ("the index logic is slightly more involved"), [CP] §2.1.
+ *   x, y: device, [B,H,S,D] of `dtype`; must not overlap.  A bit-exact row copy.
+ * The name is kept for both layouts; with RA_LAYOUT_CONTIGUOUS it is a plain copy.
+ * Errors: RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_MISALIGNED, RA_ERR_CUDA.
+ */
+ra_status ra_zigzag_permute(const void* x, void* y, int64_t B, int64_t H, int64_t S,
+                            int64_t D, ra_dtype dtype, int32_t N, ra_layout layout,
+                            void* stream);
+
+/*
+ * ra_unpermute — the inverse: y[b,h,g,:] = x[b,h,inv(g),:] (shard-major -> original).
+ * Same arguments, layout and errors as ra_zigzag_permute.
+ */
+ra_status ra_unpermute(const void* x, void* y, int64_t B, int64_t H, int64_t S,
+                       int64_t D, ra_dtype dtype, int32_t N, ra_layout layout,
+                       void* stream);
+
+/*
+ * ra_forward — exact softmax attention over N virtual ring shards.
+ * [ZZ] §Zig Zag (each shard's Q meets every K/V block in ring-step order: at step
+ * t shard r meets the K/V of shard (r-t) mod N), [CP] §3.1, [LC] §3.1.2 (blockwise
+ * evaluation with running max m and running sum l; partials across ring steps are
+ * merged through the log-sum-exp), [LC] §2.1.2 (scale and ALiBi).
+ *   q, k, v:  device, [B,H,S,D] `dtype`, shard-major order.
+ *   o:        device, [B,H,S,D] `dtype`, shard-major order (written).
+ *   lse:      device, fp32 [B,H,S], shard-major (written): natural-log
+ *             log-sum-exp of each row's scaled, biased, visible scores.
+ *   causal:   nonzero -> key j is visible to query i iff g(j) <= g(i), g = global
+ *             position (diagonal visible).
+ *   alibi_slopes: device fp32 [H] or NULL; adds -|g(i)-g(j)| * slopes[h] to the
+ *             scaled score.
+ *   softmax_scale: <= 0 selects 1/sqrt(D).
+ * bf16 runs on the tensor cores (fp32 accumulation, P rounded to bf16 for the PV
+ * product); fp32 runs in exact fp32 arithmetic on the CUDA cores.
+ * Errors: RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_MISALIGNED, RA_ERR_CUDA.
+ */
+ra_status ra_forward(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int64_t B, int64_t H, int64_t S, int64_t D, ra_dtype dtype,
+                     int32_t causal, const float* alibi_slopes, float softmax_scale,
+                     int32_t N, ra_layout layout, void* stream);
+
+/*
+ * ra_backward_workspace_bytes — device scratch ra_backward needs for these sizes:
+ * an fp32 [B,H,S] row term D_i = dO_i . O_i and an fp32 [B,H,S,D] dQ accumulator,
+ * each 256-byte aligned.  Returns 0 for an empty problem.
+ */
+size_t ra_backward_workspace_bytes(int64_t B, int64_t H, int64_t S, int64_t D);
+
+/*
+ * ra_backward — dQ, dK, dV of ra_forward, recomputing each block's probabilities
+ * from the saved LSE ([LC] §3.1.2 recompute strategy).  The gradient equations are
+ * the analytic derivative of the forward (the pages give none):
+ *   D_i = dO_i.O_i;  P_ij = exp(s_ij - LSE_i);  dS_ij = P_ij (dO_i.V_j - D_i);
+ *   dV_j = sum_i P_ij dO_i;  dQ_i = scale sum_j dS_ij K_j;  dK_j = scale sum_i dS_ij Q_i.
+ *   q, k, v, o, dout: device [B,H,S,D] `dtype`, shard-major; lse: device fp32
+ *   [B,H,S] from ra_forward with the same arguments.
+ *   dq, dk, dv: device [B,H,S,D] `dtype`, shard-major (written).
+ *   workspace: device, >= ra_backward_workspace_bytes(B,H,S,D) bytes, 256-byte
+ *   aligned, caller-owned; its contents on entry do not matter.
+ * Other arguments as ra_forward.  ALiBi slopes and the mask get no gradient.
+ * Errors: as ra_forward, plus RA_ERR_WORKSPACE.
+ */
+ra_status ra_backward(const void* q, const void* k, const void* v, const void* o,
+                      const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                      void* workspace, size_t workspace_bytes,
+                      int64_t B, int64_t H, int64_t S, int64_t D, ra_dtype dtype,
+                      int32_t causal, const float* alibi_slopes, float softmax_scale,
+                      int32_t N, ra_layout layout, void* stream);
+
+/* ra_status_string — a static, human-readable name for a status code. */
+const char* ra_status_string(ra_status status);
+
+/*
+ * ra_check_device_status — synchronises `stream`, then reads and clears the device
+ * status word.  Returns RA_ERR_TIMEOUT if a kernel gave up on a bounded wait since
+ * the last check (its outputs are then not valid), RA_ERR_CUDA on a CUDA error,
+ * RA_OK otherwise.  `detail_host` (may be NULL) receives 4 int32: code, kernel id,
+ * block index, wait site.
+ */
+ra_status ra_check_device_status(void* stream, int32_t* detail_host);
+
+/*
+ * ra_forward_path — which kernel ra_forward would run for these arguments:
+ * 1 = tensor-core (tcgen05) kernel, 2 = CUDA-core fp32 kernel, 0 = nothing to do,
+ * a negative ra_status if the arguments would be rejected.  Host only, no launch.
+ */
+int32_t ra_forward_path(int64_t B, int64_t H, int64_t S, int64_t D, ra_dtype dtype,
+                        int32_t N, ra_layout layout);
+
+/*
+ * ra_debug_wait_timeout — failure-detection self test.  Launches one block whose
+ * warp waits on an mbarrier that nothing ever arrives on, with a limit of
+ * `limit_us` microseconds; the wait gives up, records RA_ERR_TIMEOUT in the device
+ * status word and the kernel returns normally (no trap, no fault).  A following
+ * ra_check_device_status must report RA_ERR_TIMEOUT.
+ */
+ra_status ra_debug_wait_timeout(int32_t limit_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RA_H_ */

@@ -1,0 +1,92 @@
+"""The C ABI on the host: the library loads, exports every declared entry point,
+and the host-only calls and argument checks behave as include/ra.h states.
+No kernel is launched here."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from context_ra_forward_gb300 import build, binding
+    build.build()
+    return binding.lib()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "ra.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ra_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_symbols()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    assert L.ra_status_string(0) == b"RA_OK"
+    assert L.ra_status_string(-5) == b"RA_ERR_TIMEOUT"
+    assert L.ra_status_string(123) == b"RA_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("S,N,layout", [(16, 2, "zigzag"), (1024, 4, "zigzag"), (96, 3, "contiguous"),
+                                        (65536, 8, "zigzag"), (24, 12, "zigzag"), (10, 1, "contiguous")])
+def test_index_map_matches_oracle_bit_exact(L, S, N, layout):
+    from context_ra_forward_gb300 import binding
+    perm, inv = binding.index_map(S, N, layout)
+    operm, oinv = oracle.index_maps(S, N, layout)
+    assert np.array_equal(perm, operm) and np.array_equal(inv, oinv)
+
+
+def test_index_map_rejects(L):
+    buf = np.empty(16, dtype=np.int64)
+    assert L.ra_index_map(12, 4, 1, buf.ctypes.data, None) == -1   # 12 % 8 != 0
+    assert L.ra_index_map(10, 3, 0, buf.ctypes.data, None) == -1
+    assert L.ra_index_map(8, 0, 0, buf.ctypes.data, None) == -1
+    assert L.ra_index_map(8, 2, 7, buf.ctypes.data, None) == -2
+    assert L.ra_index_map(0, 2, 1, None, None) == 0
+
+
+def test_workspace_bytes(L):
+    assert L.ra_backward_workspace_bytes(0, 1, 128, 128) == 0
+    got = L.ra_backward_workspace_bytes(1, 2, 300, 64)
+    rows = 600
+    assert got == ((rows * 4 + 255) // 256) * 256 + ((rows * 64 * 4 + 255) // 256) * 256
+
+
+def test_forward_path_and_validation(L):
+    # argument checks run before any CUDA call, so they work without a GPU
+    f = L.ra_forward_path
+    assert f(1, 2, 1000, 96, 1, 4, 1) == -2       # D unsupported
+    assert f(1, 2, 1000, 128, 1, 3, 1) == -1      # 1000 % 6
+    assert f(1, 2, 1000, 128, 5, 4, 1) == -2      # dtype
+    assert f(0, 2, 1024, 128, 1, 4, 1) == 0       # empty
+    assert f(1, 2, 1024, 64, 0, 4, 1) == 2        # fp32 -> CUDA-core kernel
+    fwd = L.ra_forward
+    vp = ctypes.c_void_p(16)
+    # zero-size problem: nothing to do, no launch, even with NULL pointers
+    assert fwd(None, None, None, None, None, 1, 2, 0, 128, 1, 1, None, ctypes.c_float(0.0), 4, 1, None) == 0
+    assert fwd(None, None, None, None, None, 1, 2, 64, 128, 1, 1, None, ctypes.c_float(0.0), 4, 1, None) == -1
+    assert fwd(vp, vp, vp, ctypes.c_void_p(1 << 20), vp, 1, 2, 64, 100, 1, 1, None, ctypes.c_float(0.0), 4, 1, None) == -2
+    mis = ctypes.c_void_p(8)
+    assert fwd(mis, vp, vp, ctypes.c_void_p(1 << 20), vp, 1, 2, 64, 128, 1, 1, None, ctypes.c_float(0.0), 4, 1, None) == -3
+    # permute: aliasing input and output is rejected
+    assert L.ra_zigzag_permute(vp, vp, 1, 1, 64, 128, 1, 4, 1, None) == -1
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    from context_ra_forward_gb300 import binding
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError):
+        binding.lib()

@@ -1,0 +1,32 @@
+"""ra_backward on the GPU against the oracle's analytic gradient."""
+import numpy as np
+import pytest
+
+import oracle
+from context_ra_forward_gb300 import inputs
+from gpu_util import compare, run_case
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # (name, dtype, causal, alibi, N, layout, B, H, S, D)
+    ("c5_reduced", "bf16", True, False, 16, "zigzag", 1, 2, 4096, 128),
+    ("c5_alibi", "bf16", True, True, 4, "zigzag", 1, 2, 2048, 128),
+    ("noncausal", "bf16", False, False, 2, "contiguous", 1, 2, 1024, 128),
+    ("ragged", "bf16", True, False, 3, "zigzag", 1, 2, 1200, 128),
+    ("tail", "bf16", True, True, 4, "contiguous", 1, 1, 1000, 128),
+    ("d64", "bf16", True, False, 2, "zigzag", 1, 2, 512, 64),
+    ("f32", "f32", True, True, 4, "zigzag", 1, 2, 1024, 64),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_backward_parity(case):
+    name, dt, causal, alibi, N, layout, B, H, S, D = case
+    w = inputs.Workload(name, B, H, S, D, dt, causal, alibi, N, layout, True, 17)
+    out, f64, slopes, scale = run_case(w)
+    dq, dk, dv = oracle.attention_backward(f64["q"], f64["k"], f64["v"], f64["do"], causal=causal,
+                                           scale=scale, slopes=slopes)
+    compare(out["dq"], dq, dt, "dQ")
+    compare(out["dk"], dk, dt, "dK")
+    compare(out["dv"], dv, dt, "dV")

@@ -1,0 +1,116 @@
+"""ra_forward on the GPU against the fp64 oracle, element by element, on seeded
+inputs; cross-layout and cross-N consistency; edge cases."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from context_ra_forward_gb300 import inputs
+from gpu_util import compare, run_case, to_orig
+
+pytestmark = pytest.mark.gpu
+
+W = inputs.WORKLOADS
+
+
+def _check_forward(w, **sizes):
+    out, f64, slopes, scale = run_case(w, backward=False, **sizes)
+    o_ref, l_ref = oracle.attention_forward(f64["q"], f64["k"], f64["v"], causal=w.causal,
+                                            scale=scale, slopes=slopes)
+    a = compare(out["o"], o_ref, w.dtype, "O")
+    b = compare(out["lse"], l_ref, w.dtype, "LSE")
+    return a, b
+
+
+def test_c1_full_fp32():
+    """C1 in full: fp32, causal, B1 H2 S1024 D64, N=4 zig-zag; max abs <= 1e-4."""
+    _check_forward(W["C1"])
+
+
+@pytest.mark.parametrize("cfg,S,H", [("C2", 2048, 2), ("C3", 2048, 2), ("C4", 2048, 3), ("C5", 4096, 1)])
+def test_bf16_reduced(cfg, S, H):
+    """The bf16 configurations at a size the oracle finishes in seconds (same
+    layout and N, several tiles per shard)."""
+    _check_forward(W[cfg], S=S, H=H)
+
+
+RAGGED = [
+    # (name, dtype, causal, alibi, N, layout, B, H, S, D)
+    ("zz_h200", "bf16", True, False, 3, "zigzag", 1, 2, 1200, 128),     # chunks of 200: tiles straddle
+    ("ct_c250", "bf16", True, True, 4, "contiguous", 2, 1, 1000, 128),  # ragged tail (1000 % 128)
+    ("zz_h1", "bf16", True, True, 4, "zigzag", 1, 2, 8, 128),           # one token per chunk
+    ("tiny", "bf16", False, False, 1, "zigzag", 1, 1, 2, 128),
+    ("nc_alibi", "bf16", False, True, 2, "zigzag", 1, 2, 640, 128),     # symmetric ALiBi
+    ("d64_bf16", "bf16", True, True, 2, "zigzag", 1, 2, 512, 64),
+    ("f32_d128", "f32", True, True, 2, "zigzag", 1, 2, 384, 128),
+    ("f32_nc", "f32", False, False, 3, "contiguous", 1, 2, 300, 64),
+    ("n_eq_half_s", "bf16", True, False, 64, "zigzag", 1, 1, 256, 128),  # chunk = 2 tokens
+    ("batch_heads", "bf16", True, False, 2, "zigzag", 3, 5, 512, 128),
+]
+
+
+@pytest.mark.parametrize("case", RAGGED, ids=[c[0] for c in RAGGED])
+def test_edge_cases(case):
+    name, dt, causal, alibi, N, layout, B, H, S, D = case
+    w = inputs.Workload(name, B, H, S, D, dt, causal, alibi, N, layout, False, 13)
+    _check_forward(w)
+
+
+def test_layout_and_n_independence():
+    """O and LSE in original order do not depend on N or the layout (the ring is
+    a visit order; the merge is exact up to rounding)."""
+    base = None
+    for N, layout in [(1, "contiguous"), (8, "zigzag"), (4, "contiguous"), (16, "zigzag")]:
+        w = inputs.Workload("x", 1, 2, 4096, 128, "bf16", True, False, N, layout, False, 21)
+        out, _, _, _ = run_case(w, backward=False)
+        if base is None:
+            base = out
+            continue
+        for n in ("o", "lse"):
+            assert np.max(np.abs(out[n] - base[n])) <= 2e-2
+
+
+def test_custom_scale():
+    w = inputs.Workload("s", 1, 2, 512, 128, "bf16", True, False, 2, "zigzag", False, 3)
+    import context_ra_forward_gb300 as ra
+    x = inputs.make_inputs(w)
+    q, k, v = (ra.zigzag_permute(x[n].cuda(), w.N, w.layout) for n in ("q", "k", "v"))
+    o, lse = ra.forward(q, k, v, causal=True, softmax_scale=0.05, N=w.N, layout=w.layout)
+    perm, _ = oracle.index_maps(w.S, w.N, w.layout)
+    f = {n: inputs.to_f64_numpy(t) for n, t in x.items()}
+    o_ref, l_ref = oracle.attention_forward(f["q"], f["k"], f["v"], causal=True, scale=0.05)
+    compare(to_orig(o, perm), o_ref, "bf16", "O")
+    compare(to_orig(lse, perm), l_ref, "bf16", "LSE")
+
+
+def test_empty_problem():
+    import context_ra_forward_gb300 as ra
+    q = torch.empty((1, 2, 0, 128), dtype=torch.bfloat16, device="cuda")
+    o, lse = ra.forward(q, q, q, causal=True, N=4, layout="zigzag")
+    assert o.shape == q.shape and lse.shape == (1, 2, 0)
+
+
+def test_rejects_bad_arguments():
+    import context_ra_forward_gb300 as ra
+    q = torch.zeros((1, 2, 1000, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ra.RAError) as e:
+        ra.forward(q, q, q, causal=True, N=3, layout="zigzag")  # 1000 % 6
+    assert e.value.status == -1
+    q96 = torch.zeros((1, 2, 64, 96), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ra.RAError) as e:
+        ra.forward(q96, q96, q96, N=1)
+    assert e.value.status == -2
+
+
+def test_non_finite_input_propagates():
+    """A NaN in K reaches every row that sees it and no other (exact masking)."""
+    import context_ra_forward_gb300 as ra
+    w = inputs.Workload("nan", 1, 1, 512, 128, "bf16", True, False, 2, "contiguous", False, 4)
+    x = inputs.make_inputs(w)
+    x["k"][0, 0, 300, 5] = float("nan")
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))  # N=2 contiguous: identity map
+    o, lse = ra.forward(q, k, v, causal=True, N=2, layout="contiguous")
+    bad = torch.isnan(o[0, 0]).any(dim=-1).cpu().numpy()
+    assert not bad[:300].any() and bad[300:].all()
