@@ -141,6 +141,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Waits for the phase with the given parity to complete, at most `limit_ns`.
 // On expiry records RA_ERR_TIMEOUT and returns false; the caller then stops its
 // work and falls through to the kernel's teardown (no trap, no endless loop).
+// A wait also gives up as soon as the status word holds a failure, so one lost
+// signal ends the whole launch quickly; the word stays set (and later waits keep
+// giving up) until the host reads and clears it.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* status,
                                           int32_t kernel, int32_t site,
                                           uint64_t limit_ns = kWaitLimitNs) {
@@ -150,6 +153,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
+    if (status != nullptr && *reinterpret_cast<volatile int32_t*>(status) != 0) return false;
     if (globaltimer_ns() - t0 > limit_ns) {
       record_failure(status, RA_ERR_TIMEOUT, kernel, site);
       return false;

@@ -1,11 +1,557 @@
-// ra_fwd_tc.cu — tcgen05 tensor-core forward (bf16, D = 128).
+// ra_fwd_tc.cu — tcgen05 tensor-core forward for bf16, head dim 128.
+//
+// Pages cited:
+//   [ZZ] "大模型如何訓練百萬 Token 上下文：上下文并行與 Ring Attention" §Zig Zag Ring
+//        Attention: the Q block of shard r meets the K/V of shard (r - t) mod N at
+//        ring step t until it has met every K/V block; zig-zag assignment balances
+//        causal work, fully masked blocks need not be computed.
+//   [LC] "超长上下文技术" survey §3.1.2 (blockwise attention with a running row max
+//        m and sum l; output rescaled when m grows) and §2.1.2 (scale 1/sqrt(d),
+//        ALiBi bias -|i-j| * slope after scaling).
+//
+// One CTA owns 256 consecutive shard-major query rows (two 128-row Q tiles A, B)
+// of one (batch, head) and walks the K/V tiles in ring order, skipping tiles that
+// are fully masked for both Q tiles.  The (m, l, O) state carries across ring
+// steps, which is the online log-sum-exp merge of the per-step partial results.
+//
+// Warp roles (320 threads):
+//   warps 0-3  softmax for Q tile A (thread = row; TMEM lanes 0..127)
+//   warps 4-7  softmax for Q tile B
+//   warp  8    TMA producer: Q once, then K and V tiles into 2-stage rings
+//   warp  9    TMEM allocation and MMA issue (one thread)
+// TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512),
+// all fp32 with row i in lane i.  The softmax writes P (bf16 pairs) over the
+// first 64 columns of its S tile, and the PV product reads it from there.
+//
+// MMA issue order per K/V tile j (ping-pong, so one softmax warpgroup always has
+// its scores while the tensor core works for the other):
+//   PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
+// Each S(j+1) commit therefore also certifies PV(j) complete, which is what lets
+// the softmax rescale O in TMEM right after it sees S(j+1).
+//
+// The running max is only moved when a tile's max exceeds it by more than 8 (log2
+// units); otherwise probabilities are taken against the stale max (<= 2^8).  O and
+// l use the same reference, so the final O / l and LSE are exact.
+#include <cuda.h>
+#include <math.h>
+#include <mutex>
+
 #include "ra_common.cuh"
 #include "ra_kernels.h"
+#include "ra_tc.cuh"
 
 namespace ra {
 
-bool fwd_tc_supported(int64_t, int64_t, int32_t) { return false; }
+namespace {
 
-cudaError_t launch_fwd_tc(const AttnArgs&, void*, float*, cudaStream_t) { return cudaErrorNotSupported; }
+constexpr int kBM = 128;
+constexpr int kD = 128;
+constexpr int kStages = 2;
+constexpr int kTileBytes = kBM * kD * 2;  // one 128 x 128 bf16 tile: 32 KB
+constexpr int kBoxBytes = kTileBytes / 2; // one 128 x 64 box: 16 KB
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;
+
+// Shared memory map (offsets from a 1024-byte aligned base).
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = kOffQ + 2 * kTileBytes;
+constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
+constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
+enum Bar {
+  kBarQFull = 0,
+  kBarKFull = 1,                  // + stage
+  kBarKEmpty = kBarKFull + kStages,
+  kBarVFull = kBarKEmpty + kStages,
+  kBarVEmpty = kBarVFull + kStages,
+  kBarSFull = kBarVEmpty + kStages,  // + Q tile
+  kBarPFull = kBarSFull + 2,
+  kBarODone = kBarPFull + 2,
+  kBarFinal = kBarODone + 2,
+  kNumBars = kBarFinal + 1
+};
+constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
+constexpr uint32_t kOffGtab = kOffTmemSlot + 16;            // 8 warps x 128 int32 key positions
+constexpr uint32_t kSmemBytes = kOffGtab + 8 * kBM * 4 + 1024;  // + alignment slack
+
+constexpr uint32_t kIdescS = tc::idesc_bf16(128, 128, 0, 0);   // Q (K-major) x K (K-major)
+constexpr uint32_t kIdescPV = tc::idesc_bf16(128, 128, 0, 1);  // P (TMEM) x V (MN-major)
+
+struct FwdParams {
+  SeqMap map;
+  int64_t S;
+  int32_t H;
+  int32_t BH;
+  int32_t causal;
+  int32_t aligned;      // every 256-row query pair and 128-row tile lies in one chunk
+  int32_t heavy_first;  // causal + aligned: CTAs ordered by decreasing work
+  const float* slopes;
+  float c2;             // softmax scale * log2(e)
+  __nv_bfloat16* o;
+  float* lse;
+  int32_t* status;
+};
+
+struct TileInfo {
+  int64_t p0;    // first shard-major slot of the K/V tile
+  int64_t gk0;   // global position of p0 when the tile is contiguous
+  int64_t gmin, gmax;
+  int32_t valid; // rows of the tile below S
+  bool contig;   // consecutive global positions
+};
+
+// Walks the K/V tiles of one query pair in ring order, skipping tiles every key
+// of which lies in the future of every query of the pair.  Every role of the CTA
+// runs its own copy in lockstep.
+struct KvWalk {
+  const FwdParams* P;
+  int64_t qgmax;
+  int32_t r0;
+  int32_t t;
+  int32_t seg;
+  int64_t ti, tend;
+  int64_t seg_p0, seg_g0;
+
+  __device__ void init(const FwdParams* p, int64_t qgmax_, int32_t r0_) {
+    P = p;
+    qgmax = qgmax_;
+    r0 = r0_;
+    t = -1;
+    seg = 1;  // forces a step to (t = 0, seg = 0)
+    ti = tend = 0;
+    seg_p0 = seg_g0 = 0;
+  }
+
+  __device__ bool next(TileInfo& out) {
+    const SeqMap& m = P->map;
+    if (P->aligned) {
+      const int32_t nseg = m.layout == RA_LAYOUT_ZIGZAG ? 2 : 1;
+      while (ti >= tend) {
+        if (++seg >= nseg) {
+          seg = 0;
+          if (++t >= m.N) return false;
+        }
+        const int32_t s = (r0 - t + m.N) % m.N;  // ring step t meets shard (r0 - t) mod N
+        int64_t len;
+        if (m.layout == RA_LAYOUT_ZIGZAG) {
+          len = m.h;
+          seg_p0 = s * m.c + seg * m.h;
+          seg_g0 = seg == 0 ? s * m.h : (2 * (int64_t)m.N - 1 - s) * m.h;
+        } else {
+          len = m.c;
+          seg_p0 = s * m.c;
+          seg_g0 = seg_p0;
+        }
+        int64_t cnt = len / kBM;
+        if (P->causal) {
+          const int64_t vis = qgmax < seg_g0 ? 0 : (qgmax - seg_g0) / kBM + 1;
+          cnt = vis < cnt ? vis : cnt;
+        }
+        ti = 0;
+        tend = cnt;
+      }
+      out.p0 = seg_p0 + ti * kBM;
+      out.gk0 = seg_g0 + ti * kBM;
+      out.gmin = out.gk0;
+      out.gmax = out.gk0 + kBM - 1;
+      out.valid = kBM;
+      out.contig = true;
+      ++ti;
+      return true;
+    }
+    // General shapes: tiles aligned to the buffer, owned by the shard of their first row.
+    while (true) {
+      while (ti >= tend) {
+        if (++t >= m.N) return false;
+        const int32_t s = (r0 - t + m.N) % m.N;
+        ti = (s * m.c + kBM - 1) / kBM;
+        tend = ((s + 1) * m.c + kBM - 1) / kBM;
+      }
+      const int64_t p0 = ti * kBM;
+      ++ti;
+      const int64_t p1 = p0 + kBM < P->S ? p0 + kBM : P->S;
+      int64_t gmin, gmax;
+      m.grange(p0, p1, gmin, gmax);
+      if (P->causal && gmin > qgmax) continue;
+      out.p0 = p0;
+      out.contig = m.contiguous_range(p0, p1);
+      out.gk0 = out.contig ? m.g(p0) : -1;
+      out.gmin = gmin;
+      out.gmax = gmax;
+      out.valid = (int32_t)(p1 - p0);
+      return true;
+    }
+  }
+};
+
+__device__ __forceinline__ void issue_s(uint32_t tmem, uint32_t sbase, int X, int ks) {
+  const uint32_t qa = sbase + kOffQ + X * kTileBytes;
+  const uint32_t kb = sbase + kOffK + ks * kTileBytes;
+#pragma unroll
+  for (int kk = 0; kk < kD / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+    const uint64_t a = tc::smem_desc(qa + off, 16, 1024);
+    const uint64_t b = tc::smem_desc(kb + off, 16, 1024);
+    tc::mma_ss(tmem + X * 128, a, b, kIdescS, kk > 0 ? 1u : 0u);
+  }
+}
+
+__device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t sbase, int X, int vs, bool acc) {
+  const uint32_t vb = sbase + kOffV + vs * kTileBytes;
+#pragma unroll
+  for (int kk = 0; kk < kBM / 16; ++kk) {
+    // V is [kv rows, d] with d contiguous: MN-major B.  16 kv rows per step
+    // (2048 bytes), the two 64-wide d halves are one box (16 KB) apart.
+    const uint64_t b = tc::smem_desc(vb + kk * 2048, kBoxBytes, 1024);
+    tc::mma_ts(tmem + 256 + X * 128, tmem + X * 128 + kk * 8, b, kIdescPV, (acc || kk > 0) ? 1u : 0u);
+  }
+}
+
+__global__ void __maxnreg__(200)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ FwdParams P) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* sgen = smem_raw + (sbase - raw);
+  auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * (uint32_t)i; };
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sgen + kOffTmemSlot);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const SeqMap& m = P.map;
+  const int64_t S = P.S;
+
+  // Work item: pair index (heaviest first when causal and aligned) and (b, h).
+  const int64_t L = blockIdx.x;
+  const int64_t pair = L / P.BH;
+  const int64_t bh = L - pair * P.BH;
+  const int hh = (int)(bh % P.H);
+  const int64_t P0 = P.heavy_first ? m.inv(S - 256 * (pair + 1)) : 256 * pair;
+  const int64_t qend = P0 + 256 < S ? P0 + 256 : S;
+  int64_t pair_gmin, pair_gmax;
+  m.grange(P0, qend, pair_gmin, pair_gmax);
+  const int32_t r0 = m.shard(P0);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNumBars; ++i) {
+      uint32_t cnt = 1;
+      if (i == kBarPFull || i == kBarPFull + 1) cnt = 128;
+      mbar_init(bar(i), cnt);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kMmaWarp) {
+    tc::tmem_alloc(sbase + kOffTmemSlot, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      tc::tma_prefetch_desc(&tm_q);
+      tc::tma_prefetch_desc(&tm_k);
+      tc::tma_prefetch_desc(&tm_v);
+      const int32_t z = (int32_t)bh;
+      mbar_arrive_expect_tx(bar(kBarQFull), 2 * kTileBytes);
+      for (int X = 0; X < 2; ++X)
+        for (int hf = 0; hf < 2; ++hf)
+          tc::tma_load_3d(sbase + kOffQ + X * kTileBytes + hf * kBoxBytes, &tm_q, hf * 64,
+                          (int32_t)(P0 + X * kBM), z, bar(kBarQFull));
+      KvWalk walk;
+      walk.init(&P, pair_gmax, r0);
+      TileInfo tile;
+      int j = 0;          // tiles whose K load was issued
+      bool last_v = true; // whether the V load of tile j-1 was issued too
+      bool ok = true;
+      while (ok && walk.next(tile)) {
+        const int st = j % kStages;
+        const uint32_t par = ((j / kStages) & 1) ^ 1;
+        ok = mbar_wait(bar(kBarKEmpty + st), par, P.status, kKernFwdTc, kSiteKEmpty);
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(kBarKFull + st), kTileBytes);
+        for (int hf = 0; hf < 2; ++hf)
+          tc::tma_load_3d(sbase + kOffK + st * kTileBytes + hf * kBoxBytes, &tm_k, hf * 64,
+                          (int32_t)tile.p0, z, bar(kBarKFull + st));
+        ok = mbar_wait(bar(kBarVEmpty + st), par, P.status, kKernFwdTc, kSiteVEmpty);
+        if (!ok) {
+          ++j;  // the K load of this tile is in flight, its V load is not
+          last_v = false;
+          break;
+        }
+        mbar_arrive_expect_tx(bar(kBarVFull + st), kTileBytes);
+        for (int hf = 0; hf < 2; ++hf)
+          tc::tma_load_3d(sbase + kOffV + st * kTileBytes + hf * kBoxBytes, &tm_v, hf * 64,
+                          (int32_t)tile.p0, z, bar(kBarVFull + st));
+        ++j;
+      }
+      // Let every load this warp issued land before the CTA can exit.
+      mbar_wait(bar(kBarQFull), 0, P.status, kKernFwdTc, kSiteQFull);
+      for (int back = 1; back <= kStages && back <= j; ++back) {
+        const int jj = j - back;
+        const int st = jj % kStages;
+        const uint32_t par = (jj / kStages) & 1;
+        mbar_wait(bar(kBarKFull + st), par, P.status, kKernFwdTc, kSiteKFull);
+        if (last_v || back > 1) mbar_wait(bar(kBarVFull + st), par, P.status, kKernFwdTc, kSiteVFull);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      KvWalk walk;
+      walk.init(&P, pair_gmax, r0);
+      TileInfo tile;
+      bool ok = mbar_wait(bar(kBarQFull), 0, P.status, kKernFwdTc, kSiteQFull);
+      if (ok && walk.next(tile)) {
+        ok = mbar_wait(bar(kBarKFull + 0), 0, P.status, kKernFwdTc, kSiteKFull);
+        if (ok) {
+          tc::fence_after_sync();
+          issue_s(tmem, sbase, 0, 0);
+          tc::mma_commit(bar(kBarSFull + 0));
+          issue_s(tmem, sbase, 1, 0);
+          tc::mma_commit(bar(kBarSFull + 1));
+          tc::mma_commit(bar(kBarKEmpty + 0));
+        }
+        int j = 0;
+        while (ok) {
+          const bool more = walk.next(tile);
+          const int vs = j % kStages;
+          const int ks = (j + 1) % kStages;
+          ok = mbar_wait(bar(kBarVFull + vs), (j / kStages) & 1, P.status, kKernFwdTc, kSiteVFull) &&
+               mbar_wait(bar(kBarPFull + 0), j & 1, P.status, kKernFwdTc, kSitePFull);
+          if (!ok) break;
+          tc::fence_after_sync();
+          issue_pv(tmem, sbase, 0, vs, j > 0);
+          if (more) {
+            ok = mbar_wait(bar(kBarKFull + ks), ((j + 1) / kStages) & 1, P.status, kKernFwdTc, kSiteKFull);
+            if (!ok) break;
+            tc::fence_after_sync();
+            issue_s(tmem, sbase, 0, ks);
+            tc::mma_commit(bar(kBarSFull + 0));
+          } else {
+            tc::mma_commit(bar(kBarODone + 0));
+          }
+          ok = mbar_wait(bar(kBarPFull + 1), j & 1, P.status, kKernFwdTc, kSitePFull);
+          if (!ok) break;
+          tc::fence_after_sync();
+          issue_pv(tmem, sbase, 1, vs, j > 0);
+          tc::mma_commit(bar(kBarVEmpty + vs));
+          if (more) {
+            issue_s(tmem, sbase, 1, ks);
+            tc::mma_commit(bar(kBarSFull + 1));
+            tc::mma_commit(bar(kBarKEmpty + ks));
+          } else {
+            tc::mma_commit(bar(kBarODone + 1));
+            break;
+          }
+          ++j;
+        }
+      } else if (ok) {
+        tc::mma_commit(bar(kBarODone + 0));
+        tc::mma_commit(bar(kBarODone + 1));
+      }
+      // Every MMA this thread issued completes before TMEM is released.
+      tc::mma_commit(bar(kBarFinal));
+      mbar_wait(bar(kBarFinal), 0, P.status, kKernFwdTc, kSiteODone);
+      tc::fence_before_sync();
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int X = warp >> 2;
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const int64_t qp0 = P0 + X * kBM;
+    const int64_t slot = qp0 + row;
+    const bool row_ok = slot < S;
+    const int64_t gi = row_ok ? m.g(slot) : 0;
+    const bool tile_has_rows = qp0 < S;
+    int64_t qgmin = 0, qgmax = -1;
+    if (tile_has_rows) m.grange(qp0, qp0 + kBM < S ? qp0 + kBM : S, qgmin, qgmax);
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + X * 128;
+    const uint32_t t_o = tmem + lane_off + 256 + X * 128;
+    const float c2 = P.c2;
+    const bool alibi = P.slopes != nullptr;
+    const float slope2 = alibi ? P.slopes[hh] * kLog2e : 0.f;
+    volatile int32_t* gtab = reinterpret_cast<volatile int32_t*>(sgen + kOffGtab) + warp * kBM;
+
+    float m_ref = -INFINITY, l = 0.f;
+    KvWalk walk;
+    walk.init(&P, pair_gmax, r0);
+    TileInfo tile;
+    int j = 0;
+    bool ok = true;
+    while (walk.next(tile)) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarSFull + X), j & 1, P.status, kKernFwdTc, kSiteSFull));
+      if (!ok) break;
+      tc::fence_after_sync();
+      // Classify the tile for this Q tile.
+      const bool below = tile.gmax <= qgmin;              // every key at or before every query
+      const bool above = !P.causal && tile.gmin >= qgmax; // every key at or after every query
+      bool full = tile_has_rows && tile.valid == kBM && tile.contig && (P.causal ? below : true);
+      if (alibi && full && !P.causal && !(below || above)) full = false;
+      const bool fma_mode = full && !alibi;  // p = 2^(s*c2 - m) straight from the raw score
+      if (!full && !tile.contig) {
+        // Keys of this tile come from several chunks: the warp maps the 128 slots
+        // (four per lane) into its own table.
+        __syncwarp();
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int u = lane + 32 * e;
+          gtab[u] = u < tile.valid ? (int32_t)m.g(tile.p0 + u) : 0;
+        }
+        __syncwarp();
+      }
+      const float base = below ? slope2 * (float)(tile.gk0 - gi) : slope2 * (float)(gi - tile.gk0);
+      const float sl = below ? slope2 : -slope2;
+      // Score of column u in the log2 domain (-inf when masked); fma_mode keeps it raw.
+      auto score = [&](int u, float raw) -> float {
+        if (fma_mode) return raw;
+        if (full) return fmaf(raw, c2, fmaf(sl, (float)u, base));
+        const int64_t gj = tile.contig ? tile.gk0 + u : (int64_t)gtab[u];
+        const bool vis = row_ok && u < tile.valid && (!P.causal || gj <= gi);
+        float v = raw * c2;
+        if (alibi) v -= slope2 * (float)(gi > gj ? gi - gj : gj - gi);
+        return vis ? v : -INFINITY;
+      };
+      // Pass 1: the row max of this tile.
+      float mt = -INFINITY;
+      {
+        uint32_t r[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          tc::tmem_ld32(t_s + 32 * c, r);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int u = 0; u < 32; ++u) mt = fmaxf(mt, score(32 * c + u, __uint_as_float(r[u])));
+        }
+      }
+      if (fma_mode) mt *= c2;
+      // Move the reference max only when the tile's max exceeds it by > 8.
+      const bool need = mt > m_ref + kRescaleThreshold;
+      if (__any_sync(0xffffffffu, need)) {
+        const float m_new = need ? mt : m_ref;
+        const float alpha = need ? (m_ref == -INFINITY ? 0.f : tc::ex2(m_ref - m_new)) : 1.f;
+        if (j > 0) {
+          uint32_t r[32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            tc::tmem_ld32(t_o + 32 * c, r);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 32; ++u) r[u] = __float_as_uint(__uint_as_float(r[u]) * alpha);
+            tc::tmem_st32(t_o + 32 * c, r);
+          }
+        }
+        l *= alpha;
+        m_ref = m_new;
+      }
+      const float mu = m_ref == -INFINITY ? 0.f : m_ref;
+      // Pass 2: probabilities for 64 columns at a time, packed to bf16 pairs and
+      // stored over S columns that have already been read (P column k holds
+      // scores 2k, 2k+1).
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c2i = 0; c2i < 2; ++c2i) {
+          uint32_t r[32];
+          tc::tmem_ld32(t_s + 64 * hf + 32 * c2i, r);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const int col = 64 * hf + 32 * c2i + 2 * u;
+            const float a = score(col, __uint_as_float(r[2 * u]));
+            const float b = score(col + 1, __uint_as_float(r[2 * u + 1]));
+            const float pa = fma_mode ? tc::ex2(fmaf(a, c2, -mu)) : tc::ex2(a - mu);
+            const float pb = fma_mode ? tc::ex2(fmaf(b, c2, -mu)) : tc::ex2(b - mu);
+            l += pa + pb;
+            pk[16 * c2i + u] = tc::pack_bf16(pa, pb);
+          }
+        }
+        tc::tmem_st32(t_s + 32 * hf, pk);
+      }
+      tc::tmem_wait_st();
+      tc::fence_before_sync();
+      mbar_arrive(bar(kBarPFull + X));
+      ++j;
+    }
+    // ------------------------------------------------------------- epilogue
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarODone + X), 0, P.status, kKernFwdTc, kSiteODone));
+    if (ok) {
+      tc::fence_after_sync();
+      const float inv_l = l == 0.f ? 0.f : 1.f / l;  // only l == 0 means "no visible key"; NaN inputs keep l (and O) NaN
+      __nv_bfloat16* orow = P.o + (bh * S + (row_ok ? slot : 0)) * kD;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tc::tmem_ld32(t_o + 32 * c, r);
+        tc::tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          pk[u] = l != 0.f ? tc::pack_bf16(__uint_as_float(r[2 * u]) * inv_l, __uint_as_float(r[2 * u + 1]) * inv_l)
+                          : 0u;
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+      }
+      if (row_ok) P.lse[bh * S + slot] = l != 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+    }
+    tc::fence_before_sync();
+  }
+
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+bool fwd_tc_supported(int64_t S, int64_t D, int32_t dtype) {
+  return dtype == RA_BF16 && D == kD && S >= kBM;
+}
+
+cudaError_t launch_fwd_tc(const AttnArgs& a, void* o, float* lse, cudaStream_t st) {
+  const int64_t BH = a.B * a.H;
+  if (BH > INT32_MAX) return cudaErrorInvalidValue;
+  CUtensorMap tq, tk, tv;
+  if (!tc::make_tmap_bhsd(&tq, a.q, BH, a.S, a.D, kBM) || !tc::make_tmap_bhsd(&tk, a.k, BH, a.S, a.D, kBM) ||
+      !tc::make_tmap_bhsd(&tv, a.v, BH, a.S, a.D, kBM))
+    return cudaErrorInvalidValue;
+  FwdParams p;
+  p.map = a.map;
+  p.S = a.S;
+  p.H = (int32_t)a.H;
+  p.BH = (int32_t)BH;
+  p.causal = a.causal;
+  const int64_t chunk = a.map.layout == RA_LAYOUT_ZIGZAG ? a.map.h : a.map.c;
+  p.aligned = (chunk % 256) == 0;
+  p.heavy_first = p.aligned && a.causal;
+  p.slopes = a.slopes;
+  p.c2 = a.scale * kLog2e;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.status = a.status;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const int64_t pairs = (a.S + 255) / 256;
+  const int64_t blocks = pairs * BH;
+  if (blocks > INT32_MAX) return cudaErrorInvalidValue;
+  fwd_tc_kernel<<<(unsigned)blocks, kThreads, kSmemBytes, st>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
 
 }  // namespace ra

@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(AttnArgs a, T* __res
   }
 
   if (row_ok) {
-    const float inv_l = l > 0.f ? 1.f / l : 0.f;
+    const float inv_l = l == 0.f ? 0.f : 1.f / l;  // only l == 0 means "no visible key"; NaN inputs keep l (and O) NaN
     T* orow = o + (bh * S + pi) * D;
 #pragma unroll
     for (int t = 0; t < kC; ++t) {
@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(AttnArgs a, T* __res
                 make_float4(acc[4 * t] * inv_l, acc[4 * t + 1] * inv_l, acc[4 * t + 2] * inv_l,
                             acc[4 * t + 3] * inv_l));
     }
-    if (ql == 0) lse[bh * S + pi] = l > 0.f ? (mrun + log2f(l)) * kLn2 : -INFINITY;
+    if (ql == 0) lse[bh * S + pi] = l != 0.f ? (mrun + log2f(l)) * kLn2 : -INFINITY;
   }
 }
 

@@ -154,7 +154,9 @@ const char* ra_status_string(ra_status status);
  * ra_check_device_status — synchronises `stream`, then reads and clears the device
  * status word.  Returns RA_ERR_TIMEOUT if a kernel gave up on a bounded wait since
  * the last check (its outputs are then not valid), RA_ERR_CUDA on a CUDA error,
- * RA_OK otherwise.  `detail_host` (may be NULL) receives 4 int32: code, kernel id,
+ * RA_OK otherwise.  While the word holds a failure, kernels with bounded waits
+ * give up at their first wait that does not succeed at once (fail-stop), so
+ * check the status after a timeout before trusting further results.  `detail_host` (may be NULL) receives 4 int32: code, kernel id,
  * block index, wait site.
  */
 ra_status ra_check_device_status(void* stream, int32_t* detail_host);
