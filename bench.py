@@ -1,0 +1,466 @@
+#!/usr/bin/env python
+"""Benchmark of the ring / zig-zag attention hot path on one or more GB300s.
+
+One step = one pass of the whole path over one batch of synthetic input:
+permute Q, K, V, dO to shard-major order -> forward (O, LSE) -> backward (dQ, dK,
+dV) -> unpermute O, dQ, dK, dV back to original order.  Default workload: causal
+bf16 B1 H16 S262144 D128, N=16 zig-zag (forward + backward), the configuration
+whose step exercises every part of the path.  The metric is useful attention
+TFLOP/s, causal-adjusted: forward 4*B*H*S^2*D/2, backward 2.5x forward.
+
+Prints ONE JSON line (rank 0).  With --gpus N > 1 (launched by torchrun) every
+rank runs an independent replica of the workload (no data-path collective) and
+the value is the sum over ranks divided by the slowest rank's time.
+
+--impl reference times the fp64 CPU oracle on bounded samples of the same
+workload on the host cores (the only other use of the oracle here).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+METRIC = "attention TFLOP/s (causal-adjusted) and % of GB300 BF16 tensor peak, 1 GPU"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="C5", choices=["C2", "C3", "C4", "C5"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-side-configs", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline time budget")
+    return ap.parse_args()
+
+
+def flops_of(w, backward=None):
+    fwd = 4.0 * w.B * w.H * w.S * w.S * w.D * (0.5 if w.causal else 1.0)
+    bwd = 2.5 * fwd if (w.backward if backward is None else backward) else 0.0
+    return fwd, bwd
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the kernel source as it is now (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not rec:
+        return None
+    if rec.get("source_hash") != source_hash(rec.get("sources", [])):
+        return None
+    return rec
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        loaded = [s for s in sm if s > 0.5 * (mx or max(sm))] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def physical_gpu_index(local_rank):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [x for x in vis.split(",") if x.strip()]
+    if ids and all(x.strip().isdigit() for x in ids) and local_rank < len(ids):
+        return int(ids[local_rank])
+    return local_rank
+
+
+# ---------------------------------------------------------------------------
+# CPU side: the oracle on bounded samples
+# ---------------------------------------------------------------------------
+_SAMPLE_CACHE = {}
+
+
+def oracle_sample(w, budget_s, head=0):
+    """Times the fp64 oracle's forward (and dQ rows when the workload has a
+    backward) on query rows of one head, spread over all shards, until the time
+    budget is used.  Returns (TFLOP/s, description, threads, seconds)."""
+    import numpy as np
+
+    import oracle
+    from context_ra_forward_gb300 import inputs
+
+    key = (w.name, head)
+    if key not in _SAMPLE_CACHE:
+        x = inputs.make_inputs(w, B=1, H=1, seed=w.seed + head)
+        f = {n: inputs.to_f64_numpy(t) for n, t in x.items()}
+        perm, _ = oracle.index_maps(w.S, w.N, w.layout)
+        _SAMPLE_CACHE[key] = (f, perm)
+    f, perm = _SAMPLE_CACHE[key]
+    slopes = inputs.alibi_slopes(w.H).double().numpy()[head:head + 1] if w.alibi else None
+    scale = 1.0 / math.sqrt(w.D)
+    rng = np.random.default_rng(0)
+    done_rows, useful, t0 = 0, 0.0, time.perf_counter()
+    while time.perf_counter() - t0 < budget_s:
+        rows = np.sort(perm[rng.integers(0, w.S, size=16)])  # rows of random shard slots
+        oracle.attention_forward(f["q"], f["k"], f["v"], causal=w.causal, scale=scale, slopes=slopes, rows=rows)
+        vis = (rows + 1).sum() if w.causal else len(rows) * w.S
+        useful += 4.0 * w.D * vis
+        if w.backward:
+            oracle.backward_dq_rows(f["q"], f["k"], f["v"], f["do"], rows, causal=w.causal, scale=scale,
+                                    slopes=slopes)
+            useful += 6.0 * w.D * vis
+        done_rows += len(rows)
+    el = time.perf_counter() - t0
+    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    what = (f"fp64 oracle, {done_rows} query rows of head {head} drawn from all {w.N} shards of {w.name} "
+            f"(forward{' + dQ rows' if w.backward else ''}); useful flops 4D per visible pair"
+            f"{' + 6D for the dQ row' if w.backward else ''}")
+    return useful / el / 1e12, what, threads, el
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    per_step = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(w, per_step)
+    vals = []
+    t0 = time.perf_counter()
+    desc, threads = "", 0
+    for _ in range(args.steps):
+        v, desc, threads, _ = oracle_sample(w, per_step)
+        vals.append(v)
+    el = time.perf_counter() - t0
+    value = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w):
+    return {"workload": f"{w.name}: {'causal' if w.causal else 'non-causal'}{' + ALiBi' if w.alibi else ''} "
+                        f"{'forward + backward' if w.backward else 'forward'}, bf16, B{w.B} H{w.H} S{w.S} D{w.D}, "
+                        f"N={w.N} {w.layout}",
+            "B": w.B, "H": w.H, "S": w.S, "D": w.D, "N": w.N, "layout": w.layout, "causal": w.causal,
+            "alibi": w.alibi, "backward": w.backward,
+            "l2": "inputs larger than L2 (each of Q, K, V, dO is larger than the 129 MB L2)"}
+
+
+# ---------------------------------------------------------------------------
+# GPU side
+# ---------------------------------------------------------------------------
+class Path:
+    """Device buffers and one step of the path; per-phase CUDA events."""
+
+    PHASES = ("permute", "forward", "backward", "unpermute")
+
+    def __init__(self, w, dev, host_inputs=None):
+        import context_ra_forward_gb300 as ra
+        from context_ra_forward_gb300 import inputs
+        self.ra, self.w, self.dev = ra, w, dev
+        x = host_inputs if host_inputs is not None else inputs.make_inputs(w)
+        names = ["q", "k", "v"] + (["do"] if w.backward else [])
+        self.names = names
+        self.x = {n: x[n].to(dev) for n in names}                 # original order
+        self.xp = {n: torch.empty_like(self.x[n]) for n in names}  # shard-major
+        self.slopes = inputs.alibi_slopes(w.H).to(dev) if w.alibi else None
+        self.o = torch.empty_like(self.x["q"])
+        self.lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
+        self.outs = {"o": self.o}
+        if w.backward:
+            self.grads = tuple(torch.empty_like(self.x["q"]) for _ in range(3))
+            self.outs.update(dq=self.grads[0], dk=self.grads[1], dv=self.grads[2])
+            self.ws = torch.empty(max(1, ra.backward_workspace_bytes(w.B, w.H, w.S, w.D)), dtype=torch.uint8,
+                                  device=dev)
+        self.uo = {n: torch.empty_like(t) for n, t in self.outs.items()}  # original order
+        self.phase_ms = {p: 0.0 for p in self.PHASES}
+
+    def step(self, events=None):
+        ra, w = self.ra, self.w
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)] if events is not None else None
+        if ev:
+            ev[0].record()
+        for n in self.names:
+            ra.zigzag_permute(self.x[n], w.N, w.layout, out=self.xp[n])
+        if ev:
+            ev[1].record()
+        ra.forward(self.xp["q"], self.xp["k"], self.xp["v"], causal=w.causal, alibi_slopes=self.slopes, N=w.N,
+                   layout=w.layout, out=self.o, lse=self.lse)
+        if ev:
+            ev[2].record()
+        if w.backward:
+            ra.backward(self.xp["q"], self.xp["k"], self.xp["v"], self.o, self.lse, self.xp["do"], causal=w.causal,
+                        alibi_slopes=self.slopes, N=w.N, layout=w.layout, workspace=self.ws, out=self.grads)
+        if ev:
+            ev[3].record()
+        for n, t in self.outs.items():
+            ra.unpermute(t, w.N, w.layout, out=self.uo[n])
+        if ev:
+            ev[4].record()
+            events.append(ev)
+
+    def collect(self, events):
+        torch.cuda.synchronize()
+        for ev in events:
+            for i, p in enumerate(self.PHASES):
+                self.phase_ms[p] += ev[i].elapsed_time(ev[i + 1])
+
+
+def side_config(cfg, dev, iters=3):
+    """Forward-only TFLOP/s of another workload (context for the single line)."""
+    import context_ra_forward_gb300 as ra
+    from context_ra_forward_gb300 import inputs
+    w = inputs.WORKLOADS[cfg]
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed)
+    shape = (w.B, w.H, w.S, w.D)
+    q, k, v = (torch.randn(shape, generator=g, device=dev).to(torch.bfloat16) for _ in range(3))
+    sl = inputs.alibi_slopes(w.H).to(dev) if w.alibi else None
+    o, lse = ra.forward(q, k, v, causal=w.causal, alibi_slopes=sl, N=w.N, layout=w.layout)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        ra.forward(q, k, v, causal=w.causal, alibi_slopes=sl, N=w.N, layout=w.layout, out=o, lse=lse)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / iters
+    fwd, _ = flops_of(w, backward=False)
+    return {"forward_ms": round(ms, 3), "forward_tflops": round(fwd / ms / 1e9, 1)}
+
+
+def run_ours(args, w):
+    import context_ra_forward_gb300 as ra
+    from context_ra_forward_gb300 import inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    ra.lib()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    host = inputs.make_inputs(w, seed=w.seed + rank)  # every rank: its own batch
+    path = Path(w, dev, host)
+    fwd_fl, bwd_fl = flops_of(w)
+    step_flops = fwd_fl + bwd_fl
+
+    # warm-up, then verify the device status once before timing
+    for _ in range(max(3, args.warmup)):
+        path.step()
+    st, detail = ra.check_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} {detail} after warm-up")
+
+    barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(physical_gpu_index(local_rank)) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0.0)
+    launches0 = ra.kernel_launch_count()
+    events = []
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for _ in range(args.steps):
+        path.step(events)
+    t_end.record()
+    torch.cuda.synchronize()
+    barrier()
+    launches = ra.kernel_launch_count() - launches0
+    clocks = sampler.stop() if sampler else None
+    ms = t_start.elapsed_time(t_end) / args.steps
+    ms = max_over_ranks(ms)
+    path.collect(events)
+    st, detail = ra.check_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} {detail} after the timed region")
+
+    value = world * step_flops / (ms * 1e-3) / 1e12
+
+    # dominant kernel: the phase with the largest share of the step
+    phase = {p: path.phase_ms[p] / args.steps for p in Path.PHASES}
+    dom = max(phase, key=phase.get)
+    peaks, peak_kind = measured_peaks()
+    if dom in ("forward", "backward"):
+        dom_fl = fwd_fl if dom == "forward" else bwd_fl
+        achieved = dom_fl / (phase[dom] * 1e-3) / 1e12
+        peak = peaks.get("bf16_tflops_sustained") or peaks.get("bf16_tflops")
+        kname = "fwd_tc_kernel" if dom == "forward" else "bwd_tc_kernel"
+        traffic = committed_traffic(kname)
+        roof = {"bound": "tensor", "kernel": kname, "achieved": round(achieved, 1), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
+                "peak_kind": f"{peak_kind} bf16 sustained (kernel timed inside a long step)",
+                "algorithmic": f"{dom} flops per launch {dom_fl:.4e} (FlashAttention convention, causal-adjusted)"}
+    else:
+        nbytes = 2 * len(path.names if dom == "permute" else path.outs) * w.B * w.H * w.S * w.D * 2
+        achieved = nbytes / (phase[dom] * 1e-3) / 1e9
+        peak = peaks.get("hbm_gbs")
+        roof = {"bound": "hbm", "kernel": "permute_rows_kernel", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                "peak_kind": f"{peak_kind} HBM copy"}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(path, w, args, step_flops, world, max_over_ranks)
+
+    side = {}
+    if not args.no_side_configs and rank == 0:
+        for c in ("C2", "C3", "C4"):
+            if c != w.name:
+                side[c] = side_config(c, dev)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, desc, threads, el = oracle_sample(w, args.cpu_seconds)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc,
+               "seconds": round(el, 1)}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic (seeded N(0,1), rounded to bf16)", "config": workload_config(w),
+                "tokens_per_s": round(world * w.B * w.S / (ms * 1e-3), 1),
+                "pct_of_bf16_peak": round(100.0 * value / world / (peaks.get("bf16_tflops_sustained") or 1), 2),
+                "phase_ms": {p: round(t, 3) for p, t in phase.items()},
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+                "gpu_launches_per_step": launches / args.steps, "clocks": clocks,
+                "side_configs_forward_only": side or None}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(path, w, args, step_flops, world, max_over_ranks):
+    """Same step through the public API with HOST buffers: pinned-host inputs are
+    copied in and the results copied out inside the timed region."""
+    host_in = {n: torch.empty(path.x[n].shape, dtype=path.x[n].dtype, pin_memory=True) for n in path.names}
+    for n in path.names:
+        host_in[n].copy_(path.x[n])
+    host_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in path.uo.items()}
+    host_lse = torch.empty(path.lse.shape, dtype=torch.float32, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values()) + host_lse.numel() * 4
+
+    def one():
+        for n in path.names:
+            path.x[n].copy_(host_in[n], non_blocking=True)
+        path.step()
+        for n, t in path.uo.items():
+            host_out[n].copy_(t, non_blocking=True)
+        host_lse.copy_(path.lse, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+    return {"value": round(world * step_flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def main():
+    args = parse_args()
+    sys.path.insert(0, ROOT)
+    from context_ra_forward_gb300 import inputs
+    w = inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

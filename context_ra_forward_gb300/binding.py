@@ -58,6 +58,10 @@ def lib() -> ctypes.CDLL:
     L.ra_check_device_status.argtypes = [_vp, _vp]
     L.ra_forward_path.argtypes = [_i64, _i64, _i64, _i64, _i32, _i32, _i32]
     L.ra_debug_wait_timeout.argtypes = [_i32, _vp]
+    L.ra_last_cuda_error.argtypes = []
+    L.ra_last_cuda_error.restype = ctypes.c_char_p
+    L.ra_kernel_launch_count.argtypes = []
+    L.ra_kernel_launch_count.restype = ctypes.c_int64
     for name in ("ra_index_map", "ra_zigzag_permute", "ra_unpermute", "ra_forward", "ra_backward",
                  "ra_check_device_status", "ra_forward_path", "ra_debug_wait_timeout"):
         getattr(L, name).restype = ctypes.c_int32
@@ -67,6 +71,8 @@ def lib() -> ctypes.CDLL:
 
 def _check(status: int, what: str) -> None:
     if status != RA_OK:
+        if status == -4:
+            what = f"{what} [{lib().ra_last_cuda_error().decode()}]"
         raise RAError(status, what)
 
 
@@ -179,3 +185,8 @@ def check_device_status(stream=None):
 
 def debug_wait_timeout(limit_us: int, stream=None) -> None:
     _check(lib().ra_debug_wait_timeout(limit_us, _stream(stream)), "ra_debug_wait_timeout")
+
+
+def kernel_launch_count() -> int:
+    """Kernels the library has launched in this process (host-side counter)."""
+    return int(lib().ra_kernel_launch_count())

@@ -7,6 +7,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "ra_common.cuh"
@@ -60,7 +61,13 @@ bool overlaps(const void* a, const void* b, size_t bytes) {
   return x < y + bytes && y < x + bytes;
 }
 
-ra_status from_cuda(cudaError_t e) { return e == cudaSuccess ? RA_OK : RA_ERR_CUDA; }
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+ra_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return RA_OK;
+  g_last_cuda_error = e;
+  return RA_ERR_CUDA;
+}
 
 float resolve_scale(float s, int64_t D) { return s > 0.f ? s : 1.0f / sqrtf((float)D); }
 
@@ -105,9 +112,22 @@ ra_status attn_args(const void* q, const void* k, const void* v, int64_t B, int6
   return status_word(&a->status);
 }
 
+std::atomic<int64_t> g_launches{0};
+
 }  // namespace
 
+namespace ra {
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+}  // namespace ra
+
 extern "C" {
+
+int64_t ra_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* ra_last_cuda_error(void) {
+  return g_last_cuda_error == cudaSuccess ? "cudaSuccess" : cudaGetErrorName(g_last_cuda_error);
+}
+
 
 const char* ra_status_string(ra_status s) {
   switch (s) {
@@ -217,7 +237,7 @@ ra_status ra_backward(const void* q, const void* k, const void* v, const void* o
   float* dvec = static_cast<float*>(workspace);
   float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + (rows * 4 + 255) / 256 * 256);
   cudaError_t e = ra::launch_bwd_rowdot(a, o, dout, dvec, st);
-  if (e != cudaSuccess) return RA_ERR_CUDA;
+  if (e != cudaSuccess) return from_cuda(e);
   if (ra::bwd_tc_supported(S, D, dt))
     return from_cuda(ra::launch_bwd_tc(a, lse, dout, dvec, dq_acc, dq, dk, dv, st));
   return from_cuda(ra::launch_bwd_simt(a, lse, dout, dvec, dq, dk, dv, st));

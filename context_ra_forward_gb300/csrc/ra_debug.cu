@@ -27,6 +27,7 @@ __global__ void debug_wait_kernel(int32_t limit_us, int32_t* status) {
 
 cudaError_t launch_debug_wait(int32_t limit_us, int32_t* status, cudaStream_t st) {
   debug_wait_kernel<<<1, 32, 0, st>>>(limit_us, status);
+  note_launch();
   return cudaGetLastError();
 }
 

@@ -186,6 +186,83 @@ struct KvWalk {
   }
 };
 
+// Per-row context of one K/V tile for the softmax.
+struct RowCtx {
+  float c2, sl, base, slope2;
+  int64_t gi, gk0;
+  int32_t valid;
+  bool contig, causal, row_ok, alibi;
+  const volatile int32_t* gtab;
+};
+
+enum TileKind { kPlain = 0, kLinear = 1, kGeneral = 2 };
+
+// Score of column u in the log2 domain.  kPlain keeps the raw score (scaled
+// inside the exponent); kLinear adds the ALiBi bias of a tile that lies wholly
+// on one side of every query; kGeneral masks and biases element by element.
+template <int kKind>
+__device__ __forceinline__ float tile_score(int u, float raw, const RowCtx& c) {
+  if constexpr (kKind == kPlain) {
+    return raw;
+  } else if constexpr (kKind == kLinear) {
+    return fmaf(raw, c.c2, fmaf(c.sl, (float)u, c.base));
+  } else {
+    const int64_t gj = c.contig ? c.gk0 + u : (int64_t)c.gtab[u];
+    const bool vis = c.row_ok && u < c.valid && (!c.causal || gj <= c.gi);
+    float v = raw * c.c2;
+    if (c.alibi) v -= c.slope2 * (float)(c.gi > gj ? c.gi - gj : gj - c.gi);
+    return vis ? v : -INFINITY;
+  }
+}
+
+template <int kKind>
+__device__ __forceinline__ float tile_max(uint32_t t_s, const RowCtx& c) {
+  float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+  for (int ch = 0; ch < 4; ++ch) {
+    uint32_t r[32];
+    tc::tmem_ld32(t_s + 32 * ch, r);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int u = 0; u < 32; ++u) mx[u & 3] = fmaxf(mx[u & 3], tile_score<kKind>(32 * ch + u, __uint_as_float(r[u]), c));
+  }
+  const float m = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+  return kKind == kPlain ? m * c.c2 : m;
+}
+
+template <int kKind>
+__device__ __forceinline__ float tile_probs(uint32_t t_s, float mu, const RowCtx& c) {
+  float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+  for (int hf = 0; hf < 2; ++hf) {
+    uint32_t pk[32];
+#pragma unroll
+    for (int ci = 0; ci < 2; ++ci) {
+      uint32_t r[32];
+      tc::tmem_ld32(t_s + 64 * hf + 32 * ci, r);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int col = 64 * hf + 32 * ci + 2 * u;
+        const float a = tile_score<kKind>(col, __uint_as_float(r[2 * u]), c);
+        const float b = tile_score<kKind>(col + 1, __uint_as_float(r[2 * u + 1]), c);
+        float pa, pb;
+        if constexpr (kKind == kPlain) {
+          pa = tc::ex2(fmaf(a, c.c2, -mu));
+          pb = tc::ex2(fmaf(b, c.c2, -mu));
+        } else {
+          pa = tc::ex2(a - mu);
+          pb = tc::ex2(b - mu);
+        }
+        ls[u & 3] += pa + pb;
+        pk[16 * ci + u] = tc::pack_bf16(pa, pb);
+      }
+    }
+    tc::tmem_st32(t_s + 32 * hf, pk);
+  }
+  return (ls[0] + ls[1]) + (ls[2] + ls[3]);
+}
+
 __device__ __forceinline__ void issue_s(uint32_t tmem, uint32_t sbase, int X, int ks) {
   const uint32_t qa = sbase + kOffQ + X * kTileBytes;
   const uint32_t kb = sbase + kOffK + ks * kTileBytes;
@@ -209,7 +286,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t sbase, int X, i
   }
 }
 
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ FwdParams P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -394,8 +471,8 @@ __global__ void __maxnreg__(200)
       const bool above = !P.causal && tile.gmin >= qgmax; // every key at or after every query
       bool full = tile_has_rows && tile.valid == kBM && tile.contig && (P.causal ? below : true);
       if (alibi && full && !P.causal && !(below || above)) full = false;
-      const bool fma_mode = full && !alibi;  // p = 2^(s*c2 - m) straight from the raw score
-      if (!full && !tile.contig) {
+      const int kind = full ? (alibi ? kLinear : kPlain) : kGeneral;
+      if (kind == kGeneral && !tile.contig) {
         // Keys of this tile come from several chunks: the warp maps the 128 slots
         // (four per lane) into its own table.
         __syncwarp();
@@ -406,40 +483,31 @@ __global__ void __maxnreg__(200)
         }
         __syncwarp();
       }
-      const float base = below ? slope2 * (float)(tile.gk0 - gi) : slope2 * (float)(gi - tile.gk0);
-      const float sl = below ? slope2 : -slope2;
-      // Score of column u in the log2 domain (-inf when masked); fma_mode keeps it raw.
-      auto score = [&](int u, float raw) -> float {
-        if (fma_mode) return raw;
-        if (full) return fmaf(raw, c2, fmaf(sl, (float)u, base));
-        const int64_t gj = tile.contig ? tile.gk0 + u : (int64_t)gtab[u];
-        const bool vis = row_ok && u < tile.valid && (!P.causal || gj <= gi);
-        float v = raw * c2;
-        if (alibi) v -= slope2 * (float)(gi > gj ? gi - gj : gj - gi);
-        return vis ? v : -INFINITY;
-      };
-      // Pass 1: the row max of this tile.
-      float mt = -INFINITY;
-      {
-        uint32_t r[32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          tc::tmem_ld32(t_s + 32 * c, r);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int u = 0; u < 32; ++u) mt = fmaxf(mt, score(32 * c + u, __uint_as_float(r[u])));
-        }
-      }
-      if (fma_mode) mt *= c2;
+      RowCtx rc;
+      rc.c2 = c2;
+      rc.sl = below ? slope2 : -slope2;
+      rc.base = below ? slope2 * (float)(tile.gk0 - gi) : slope2 * (float)(gi - tile.gk0);
+      rc.slope2 = slope2;
+      rc.gi = gi;
+      rc.gk0 = tile.gk0;
+      rc.valid = tile.valid;
+      rc.contig = tile.contig;
+      rc.causal = P.causal != 0;
+      rc.row_ok = row_ok;
+      rc.alibi = alibi;
+      rc.gtab = gtab;
+      // Pass 1: the row max of this tile (log2 domain).
+      const float mt = kind == kPlain ? tile_max<kPlain>(t_s, rc)
+                                      : (kind == kLinear ? tile_max<kLinear>(t_s, rc) : tile_max<kGeneral>(t_s, rc));
       // Move the reference max only when the tile's max exceeds it by > 8.
       const bool need = mt > m_ref + kRescaleThreshold;
       if (__any_sync(0xffffffffu, need)) {
         const float m_new = need ? mt : m_ref;
         const float alpha = need ? (m_ref == -INFINITY ? 0.f : tc::ex2(m_ref - m_new)) : 1.f;
         if (j > 0) {
-          uint32_t r[32];
-#pragma unroll
+#pragma unroll 1
           for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
             tc::tmem_ld32(t_o + 32 * c, r);
             tc::tmem_wait_ld();
 #pragma unroll
@@ -451,30 +519,10 @@ __global__ void __maxnreg__(200)
         m_ref = m_new;
       }
       const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-      // Pass 2: probabilities for 64 columns at a time, packed to bf16 pairs and
-      // stored over S columns that have already been read (P column k holds
-      // scores 2k, 2k+1).
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int c2i = 0; c2i < 2; ++c2i) {
-          uint32_t r[32];
-          tc::tmem_ld32(t_s + 64 * hf + 32 * c2i, r);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            const int col = 64 * hf + 32 * c2i + 2 * u;
-            const float a = score(col, __uint_as_float(r[2 * u]));
-            const float b = score(col + 1, __uint_as_float(r[2 * u + 1]));
-            const float pa = fma_mode ? tc::ex2(fmaf(a, c2, -mu)) : tc::ex2(a - mu);
-            const float pb = fma_mode ? tc::ex2(fmaf(b, c2, -mu)) : tc::ex2(b - mu);
-            l += pa + pb;
-            pk[16 * c2i + u] = tc::pack_bf16(pa, pb);
-          }
-        }
-        tc::tmem_st32(t_s + 32 * hf, pk);
-      }
+      // Pass 2: probabilities, packed to bf16 pairs and stored over S columns that
+      // have already been read (P column k holds scores 2k, 2k+1).
+      l += kind == kPlain ? tile_probs<kPlain>(t_s, mu, rc)
+                          : (kind == kLinear ? tile_probs<kLinear>(t_s, mu, rc) : tile_probs<kGeneral>(t_s, mu, rc));
       tc::tmem_wait_st();
       tc::fence_before_sync();
       mbar_arrive(bar(kBarPFull + X));
@@ -551,6 +599,7 @@ cudaError_t launch_fwd_tc(const AttnArgs& a, void* o, float* lse, cudaStream_t s
   const int64_t blocks = pairs * BH;
   if (blocks > INT32_MAX) return cudaErrorInvalidValue;
   fwd_tc_kernel<<<(unsigned)blocks, kThreads, kSmemBytes, st>>>(tq, tk, tv, p);
+  note_launch();
   return cudaGetLastError();
 }
 

@@ -21,6 +21,9 @@ struct AttnArgs {
   int32_t* status;      // device status word
 };
 
+// ra_api.cu — counts every kernel launch the library makes (host side).
+void note_launch();
+
 // ra_permute.cu
 cudaError_t launch_permute(const void* x, void* y, int64_t BH, int64_t S, int64_t row_bytes,
                            const SeqMap& m, bool inverse, cudaStream_t st);

@@ -477,6 +477,7 @@ cudaError_t fwd_simt_t(const AttnArgs& a, void* o, float* lse, cudaStream_t st) 
     dim3 grid((unsigned)((a.S + kRowsPerBlock - 1) / kRowsPerBlock), (unsigned)nb);
     fwd_simt_kernel<T, D><<<grid, kThreads, smem, st>>>(sub, static_cast<T*>(o) + b0 * a.S * D,
                                                         lse + b0 * a.S);
+    note_launch();
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -506,11 +507,13 @@ cudaError_t bwd_simt_t(const AttnArgs& a, const float* lse, const void* dout, co
     dim3 grid((unsigned)((a.S + kRowsPerBlock - 1) / kRowsPerBlock), (unsigned)nb);
     bwd_dq_simt_kernel<T, D><<<grid, kThreads, smem_kv, st>>>(
         sub, lse + b0 * a.S, static_cast<const T*>(dout) + off, dvec + b0 * a.S, static_cast<T*>(dq) + off);
+    note_launch();
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     bwd_dkdv_simt_kernel<T, D><<<grid, kThreads, smem_q, st>>>(
         sub, lse + b0 * a.S, static_cast<const T*>(dout) + off, dvec + b0 * a.S,
         static_cast<T*>(dk) + off, static_cast<T*>(dv) + off);
+    note_launch();
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -523,6 +526,7 @@ cudaError_t rowdot_t(const AttnArgs& a, const void* o, const void* dout, float* 
   const int64_t blocks = (rows + 7) / 8;
   bwd_rowdot_kernel<T, D><<<(unsigned)blocks, 256, 0, st>>>(static_cast<const T*>(o),
                                                           static_cast<const T*>(dout), dvec, rows);
+  note_launch();
   return cudaGetLastError();
 }
 

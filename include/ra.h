@@ -178,6 +178,19 @@ int32_t ra_forward_path(int64_t B, int64_t H, int64_t S, int64_t D, ra_dtype dty
  */
 ra_status ra_debug_wait_timeout(int32_t limit_us, void* stream);
 
+/*
+ * ra_last_cuda_error — name of the CUDA error behind this thread's most recent
+ * RA_ERR_CUDA (a static string; "cudaSuccess" if there was none).
+ */
+const char* ra_last_cuda_error(void);
+
+/*
+ * ra_kernel_launch_count — number of kernels this library has launched in this
+ * process so far (a host-side counter, incremented at each launch).  Lets a caller
+ * count the library's launches inside a timed region.
+ */
+int64_t ra_kernel_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif
