@@ -236,10 +236,10 @@ ra_status ra_backward(const void* q, const void* k, const void* v, const void* o
   const size_t rows = (size_t)(B * H * S);
   float* dvec = static_cast<float*>(workspace);
   float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + (rows * 4 + 255) / 256 * 256);
-  cudaError_t e = ra::launch_bwd_rowdot(a, o, dout, dvec, st);
+  const bool tc = ra::bwd_tc_supported(S, D, dt, a.map) && aligned(lse, 16);
+  cudaError_t e = ra::launch_bwd_rowdot(a, o, dout, dvec, tc ? dq_acc : nullptr, st);
   if (e != cudaSuccess) return from_cuda(e);
-  if (ra::bwd_tc_supported(S, D, dt))
-    return from_cuda(ra::launch_bwd_tc(a, lse, dout, dvec, dq_acc, dq, dk, dv, st));
+  if (tc) return from_cuda(ra::launch_bwd_tc(a, lse, dout, dvec, dq_acc, dq, dk, dv, st));
   return from_cuda(ra::launch_bwd_simt(a, lse, dout, dvec, dq, dk, dv, st));
 }
 

@@ -1,14 +1,593 @@
-// ra_bwd_tc.cu — tcgen05 tensor-core backward (bf16, D = 128).
+// ra_bwd_tc.cu — tcgen05 tensor-core backward for bf16, head dim 128.
+//
+// Pages cited:
+//   [LC] "超长上下文技术" survey §3.1.2: backward recomputes intermediates (the
+//        block probabilities) instead of storing them; §2.1.2 scale and ALiBi.
+//   [ZZ] "大模型如何訓練百萬 Token 上下文：上下文并行與 Ring Attention" §Zig Zag Ring
+//        Attention: every K/V block meets every Q block, one ring step at a time.
+// The gradient itself is the analytic derivative of the forward (the pages give
+// none): with P = exp(s - LSE) and D_i = dO_i.O_i,
+//   dV_j = sum_i P_ij dO_i,  dS_ij = P_ij (dO_i.V_j - D_i),
+//   dK_j = scale sum_i dS_ij Q_i,  dQ_i = scale sum_j dS_ij K_j.
+//
+// One CTA owns one 128-row K/V tile of one (batch, head) and walks the 128-row Q
+// tiles that see it in ring order (the queries of shard (s + t) mod N at step t),
+// skipping tiles every query of which lies before every key (causal).
+//
+// Warp roles (320 threads):
+//   warps 0-7  "softmax": warp w owns K/V rows 32*(w%4).. (its TMEM lane quarter)
+//              and Q columns 64*(w/4)..: P^T, dS^T, the dQ drain, the dK/dV epilogue
+//   warp  8    TMA producer: K and V once, then Q and dO tiles into a 2-stage ring
+//   warp  9    TMEM allocation and MMA issue (one thread)
+// TMEM (512 columns): S^T [0,128), dP^T [128,256), dK [256,384), dV [384,512);
+// all fp32 with K/V row r in lane r.  P^T (bf16 pairs) is written back over S^T
+// (Q columns 0..63 -> TMEM columns 0..31, 64..127 -> 64..95), the dQ partial of
+// a Q tile (row = query) goes into the dP^T region once that has been read.
+// dS^T (bf16) goes to shared memory in the 128-byte-swizzled layout, where it is
+// the K-major A operand of dK += dS^T Q and the MN-major A operand of dQ = dS K.
+//
+// MMA order per Q tile i:  [P^T_i] dV_i  [dS^T_i] dK_i, dQ_i -> S^T_{i+1}
+//                          [dQ_i drained] dP^T_{i+1}.
+// dQ partials are added into an fp32 workspace (zeroed by the row-term pre-pass)
+// with 16-byte atomic adds; a post-pass scales and converts them.
+#include <cuda.h>
+#include <math.h>
+#include <mutex>
+
 #include "ra_common.cuh"
 #include "ra_kernels.h"
+#include "ra_tc.cuh"
 
 namespace ra {
 
-bool bwd_tc_supported(int64_t, int64_t, int32_t) { return false; }
+namespace {
 
-cudaError_t launch_bwd_tc(const AttnArgs&, const float*, const void*, const float*, float*, void*,
-                          void*, void*, cudaStream_t) {
-  return cudaErrorNotSupported;
+constexpr int kBM = 128;
+constexpr int kD = 128;
+constexpr int kTileBytes = kBM * kD * 2;   // 32 KB
+constexpr int kBoxBytes = kTileBytes / 2;  // 16 KB
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColDP = 128, kColDK = 256, kColDV = 384;
+
+// Shared memory (offsets from a 1024-byte aligned base).
+constexpr uint32_t kOffK = 0;
+constexpr uint32_t kOffV = kOffK + kTileBytes;
+constexpr uint32_t kOffQ = kOffV + kTileBytes;        // 2 stages of [Q | dO]
+constexpr uint32_t kStageBytes = 2 * kTileBytes;
+constexpr uint32_t kOffDS = kOffQ + 2 * kStageBytes;  // dS^T, 32 KB
+constexpr uint32_t kOffBar = kOffDS + kTileBytes;
+enum Bar {
+  kBarKV = 0,
+  kBarQFull = 1,  // + stage
+  kBarQEmpty = 3, // + stage
+  kBarSFull = 5,
+  kBarDPFull,
+  kBarPReady,
+  kBarDSReady,
+  kBarDSFree,
+  kBarDQFull,
+  kBarDQEmpty,
+  kBarFinal,
+  kNumBars
+};
+constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
+constexpr uint32_t kSmemUsed = kOffTmemSlot + 16;
+constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+constexpr uint32_t kIdescKK = tc::idesc_bf16(128, 128, 0, 0);  // A K-major, B K-major
+constexpr uint32_t kIdescKM = tc::idesc_bf16(128, 128, 0, 1);  // A K-major (or TMEM), B MN-major
+constexpr uint32_t kIdescMM = tc::idesc_bf16(128, 128, 1, 1);  // A MN-major, B MN-major
+
+struct BwdParams {
+  SeqMap map;
+  int64_t S;
+  int32_t H;
+  int32_t BH;
+  int32_t causal;
+  const float* slopes;
+  float c2;      // scale * log2(e)
+  float scale;
+  const float* lse;
+  const float* dvec;
+  float* dq_acc;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int32_t* status;
+};
+
+struct QTile {
+  int64_t p0;   // first shard-major slot
+  int64_t g0;   // its global position (tiles are contiguous)
+};
+
+// Q tiles that see a K/V tile, in ring order; every 128-row tile lies inside one
+// chunk (chunk length a multiple of 128), so each is a contiguous global range.
+struct QWalk {
+  const BwdParams* P;
+  int64_t kgmin;
+  int32_t s0, t, seg;
+  int64_t ti, tend, seg_p0, seg_g0;
+
+  __device__ void init(const BwdParams* p, int64_t kgmin_, int32_t s0_) {
+    P = p;
+    kgmin = kgmin_;
+    s0 = s0_;
+    t = -1;
+    seg = 1;
+    ti = tend = 0;
+    seg_p0 = seg_g0 = 0;
+  }
+  __device__ bool next(QTile& out) {
+    const SeqMap& m = P->map;
+    const int32_t nseg = m.layout == RA_LAYOUT_ZIGZAG ? 2 : 1;
+    while (ti >= tend) {
+      if (++seg >= nseg) {
+        seg = 0;
+        if (++t >= m.N) return false;
+      }
+      const int32_t s = (s0 + t) % m.N;  // step t: the queries of shard (s0 + t) mod N
+      int64_t len;
+      if (m.layout == RA_LAYOUT_ZIGZAG) {
+        len = m.h;
+        seg_p0 = s * m.c + seg * m.h;
+        seg_g0 = seg == 0 ? s * m.h : (2 * (int64_t)m.N - 1 - s) * m.h;
+      } else {
+        len = m.c;
+        seg_p0 = s * m.c;
+        seg_g0 = seg_p0;
+      }
+      tend = len / kBM;
+      ti = 0;
+      if (P->causal) {
+        if (seg_g0 + len - 1 < kgmin) {
+          tend = 0;
+        } else if (kgmin > seg_g0) {
+          ti = (kgmin - seg_g0) / kBM;
+        }
+      }
+    }
+    out.p0 = seg_p0 + ti * kBM;
+    out.g0 = seg_g0 + ti * kBM;
+    ++ti;
+    return true;
+  }
+};
+
+enum TileKind { kPlain = 0, kLinear = 1, kGeneral = 2 };
+
+// Probability P^T of K/V row gj against query column (q0g + col), log2 domain.
+struct ColCtx {
+  float c2, slope2, lin_base, lin_sl;
+  int64_t gj, q0g;
+  bool causal, alibi;
+};
+
+template <int kKind>
+__device__ __forceinline__ float prob(float s, float lse2, int col, const ColCtx& c) {
+  if constexpr (kKind == kPlain) {
+    return tc::ex2(fmaf(s, c.c2, -lse2));
+  } else if constexpr (kKind == kLinear) {
+    return tc::ex2(fmaf(s, c.c2, fmaf(c.lin_sl, (float)col, c.lin_base) - lse2));
+  } else {
+    const int64_t gi = c.q0g + col;
+    const bool vis = !c.causal || c.gj <= gi;
+    float v = s * c.c2 - lse2;
+    if (c.alibi) v -= c.slope2 * (float)(gi > c.gj ? gi - c.gj : c.gj - gi);
+    return vis ? tc::ex2(v) : 0.f;
+  }
+}
+
+// P^T for this warp's 64 query columns: from S^T in TMEM into registers (fp32)
+// and back into TMEM as bf16 pairs for the dV product.
+template <int kKind>
+__device__ __forceinline__ void compute_p(uint32_t t_row, int h, const float* lse_q, const ColCtx& c,
+                                          float (&p)[64]) {
+#pragma unroll
+  for (int ci = 0; ci < 2; ++ci) {
+    uint32_t r[32];
+    tc::tmem_ld32(t_row + kColS + 64 * h + 32 * ci, r);
+    float4 lv[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) lv[u] = __ldg(reinterpret_cast<const float4*>(lse_q + 32 * ci) + u);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int u = 0; u < 32; ++u) {
+      const float l4[4] = {lv[u >> 2].x, lv[u >> 2].y, lv[u >> 2].z, lv[u >> 2].w};
+      const float lse2 = l4[u & 3] * kLog2e;
+      p[32 * ci + u] = prob<kKind>(__uint_as_float(r[u]), lse2, 64 * h + 32 * ci + u, c);
+    }
+  }
+  uint32_t pk[32];
+#pragma unroll
+  for (int u = 0; u < 32; ++u) pk[u] = tc::pack_bf16(p[2 * u], p[2 * u + 1]);
+  tc::tmem_st32(t_row + kColS + 64 * h, pk);
+}
+
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ BwdParams P) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* sgen = smem_raw + (sbase - raw);
+  auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * (uint32_t)i; };
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sgen + kOffTmemSlot);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const SeqMap& m = P.map;
+  const int64_t S = P.S;
+
+  // Work item: K/V tile (lowest global positions first under causal: they are
+  // seen by the most queries) and (b, h).
+  const int64_t L = blockIdx.x;
+  const int64_t tile = L / P.BH;
+  const int64_t bh = L - tile * P.BH;
+  const int hh = (int)(bh % P.H);
+  const int64_t kp0 = P.causal ? m.inv(tile * kBM) : tile * kBM;
+  const int64_t kg0 = m.g(kp0);
+  const int32_t s0 = m.shard(kp0);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNumBars; ++i) {
+      uint32_t cnt = 1;
+      if (i == kBarPReady || i == kBarDSReady || i == kBarDQEmpty) cnt = 8;
+      mbar_init(bar(i), cnt);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kMmaWarp) {
+    tc::tmem_alloc(sbase + kOffTmemSlot, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      tc::tma_prefetch_desc(&tm_q);
+      tc::tma_prefetch_desc(&tm_k);
+      tc::tma_prefetch_desc(&tm_v);
+      tc::tma_prefetch_desc(&tm_do);
+      const int32_t z = (int32_t)bh;
+      mbar_arrive_expect_tx(bar(kBarKV), 2 * kTileBytes);
+      for (int hf = 0; hf < 2; ++hf) {
+        tc::tma_load_3d(sbase + kOffK + hf * kBoxBytes, &tm_k, hf * 64, (int32_t)kp0, z, bar(kBarKV));
+        tc::tma_load_3d(sbase + kOffV + hf * kBoxBytes, &tm_v, hf * 64, (int32_t)kp0, z, bar(kBarKV));
+      }
+      QWalk walk;
+      walk.init(&P, kg0, s0);
+      QTile qt;
+      int i = 0;
+      while (walk.next(qt)) {
+        const int st = i & 1;
+        if (!mbar_wait(bar(kBarQEmpty + st), ((i >> 1) & 1) ^ 1, P.status, kKernBwdTc, kSiteKEmpty)) break;
+        mbar_arrive_expect_tx(bar(kBarQFull + st), kStageBytes);
+        const uint32_t dst = sbase + kOffQ + st * kStageBytes;
+        for (int hf = 0; hf < 2; ++hf) {
+          tc::tma_load_3d(dst + hf * kBoxBytes, &tm_q, hf * 64, (int32_t)qt.p0, z, bar(kBarQFull + st));
+          tc::tma_load_3d(dst + kTileBytes + hf * kBoxBytes, &tm_do, hf * 64, (int32_t)qt.p0, z,
+                          bar(kBarQFull + st));
+        }
+        ++i;
+      }
+      // Let every load this warp issued land before the CTA can exit.
+      mbar_wait(bar(kBarKV), 0, P.status, kKernBwdTc, kSiteKFull);
+      for (int back = 1; back <= 2 && back <= i; ++back) {
+        const int ii = i - back;
+        mbar_wait(bar(kBarQFull + (ii & 1)), (ii >> 1) & 1, P.status, kKernBwdTc, kSiteQFull);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      const uint32_t kb = sbase + kOffK, vb = sbase + kOffV, dsb = sbase + kOffDS;
+      QWalk walk;
+      walk.init(&P, kg0, s0);
+      QTile qt;
+      bool ok = mbar_wait(bar(kBarKV), 0, P.status, kKernBwdTc, kSiteKFull);
+      bool more = ok && walk.next(qt);
+      if (more) {
+        ok = mbar_wait(bar(kBarQFull + 0), 0, P.status, kKernBwdTc, kSiteQFull);
+        if (ok) {
+          tc::fence_after_sync();
+          const uint32_t qb = sbase + kOffQ, dob = qb + kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {  // S^T = K Q^T
+            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+            tc::mma_ss(tmem + kColS, tc::smem_desc(kb + off, 16, 1024), tc::smem_desc(qb + off, 16, 1024),
+                       kIdescKK, kk > 0);
+          }
+          tc::mma_commit(bar(kBarSFull));
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {  // dP^T = V dO^T
+            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+            tc::mma_ss(tmem + kColDP, tc::smem_desc(vb + off, 16, 1024), tc::smem_desc(dob + off, 16, 1024),
+                       kIdescKK, kk > 0);
+          }
+          tc::mma_commit(bar(kBarDPFull));
+        }
+      }
+      int i = 0;
+      while (ok && more) {
+        const int st = i & 1;
+        const uint32_t qb = sbase + kOffQ + st * kStageBytes, dob = qb + kTileBytes;
+        ok = mbar_wait(bar(kBarPReady), i & 1, P.status, kKernBwdTc, kSitePFull);
+        if (!ok) break;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {  // dV += P^T dO   (A from TMEM)
+          const uint32_t acol = kColS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+          tc::mma_ts(tmem + kColDV, tmem + acol, tc::smem_desc(dob + kk * 2048, kBoxBytes, 1024), kIdescKM,
+                     (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        ok = mbar_wait(bar(kBarDSReady), i & 1, P.status, kKernBwdTc, kSiteBwd);
+        if (!ok) break;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {  // dK += dS^T Q   (A K-major, B MN-major)
+          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+          tc::mma_ss(tmem + kColDK, tc::smem_desc(dsb + off, 16, 1024),
+                     tc::smem_desc(qb + kk * 2048, kBoxBytes, 1024), kIdescKM, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {  // dQ_i = dS K   (A = dS^T MN-major, B = K MN-major)
+          tc::mma_ss(tmem + kColDP, tc::smem_desc(dsb + kk * 2048, kBoxBytes, 1024),
+                     tc::smem_desc(kb + kk * 2048, kBoxBytes, 1024), kIdescMM, kk > 0);
+        }
+        tc::mma_commit(bar(kBarDSFree));
+        tc::mma_commit(bar(kBarDQFull));
+        tc::mma_commit(bar(kBarQEmpty + st));
+        more = walk.next(qt);
+        if (!more) break;
+        const int nst = (i + 1) & 1;
+        const uint32_t nqb = sbase + kOffQ + nst * kStageBytes, ndob = nqb + kTileBytes;
+        ok = mbar_wait(bar(kBarQFull + nst), ((i + 1) >> 1) & 1, P.status, kKernBwdTc, kSiteQFull);
+        if (!ok) break;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+          tc::mma_ss(tmem + kColS, tc::smem_desc(kb + off, 16, 1024), tc::smem_desc(nqb + off, 16, 1024),
+                     kIdescKK, kk > 0);
+        }
+        tc::mma_commit(bar(kBarSFull));
+        ok = mbar_wait(bar(kBarDQEmpty), i & 1, P.status, kKernBwdTc, kSiteODone);
+        if (!ok) break;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+          tc::mma_ss(tmem + kColDP, tc::smem_desc(vb + off, 16, 1024), tc::smem_desc(ndob + off, 16, 1024),
+                     kIdescKK, kk > 0);
+        }
+        tc::mma_commit(bar(kBarDPFull));
+        ++i;
+      }
+      // dK/dV complete (and every MMA issued) before the epilogue and TMEM release.
+      tc::mma_commit(bar(kBarFinal));
+      mbar_wait(bar(kBarFinal), 0, P.status, kKernBwdTc, kSiteODone);
+      tc::fence_before_sync();
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------- softmax warps
+    const int qd = warp & 3;   // TMEM lane quarter: K/V rows 32*qd ..
+    const int h = warp >> 2;   // Q column half: 64*h ..
+    const int krow = qd * 32 + lane;
+    const uint32_t t_row = tmem + ((uint32_t)(qd * 32) << 16);
+    const int64_t gj = kg0 + krow;  // K/V tiles are contiguous
+    const bool alibi = P.slopes != nullptr;
+    const float slope2 = alibi ? P.slopes[hh] * kLog2e : 0.f;
+    ColCtx cc;
+    cc.c2 = P.c2;
+    cc.slope2 = slope2;
+    cc.gj = gj;
+    cc.causal = P.causal != 0;
+    cc.alibi = alibi;
+    uint8_t* ds_tile = sgen + kOffDS + h * kBoxBytes;
+    const float* lse_bh = P.lse + bh * S;
+    const float* dvec_bh = P.dvec + bh * S;
+    float* dq_bh = P.dq_acc + bh * S * kD;
+
+    QWalk walk;
+    walk.init(&P, kg0, s0);
+    QTile qt;
+    int i = 0;
+    bool ok = true;
+    while (walk.next(qt)) {
+      // Tile kind for this K/V row block against this Q tile.
+      const int64_t qgmin = qt.g0, qgmax = qt.g0 + kBM - 1;
+      const int64_t kgmin = kg0, kgmax = kg0 + kBM - 1;
+      const bool below = kgmax <= qgmin;                 // every key at or before every query
+      const bool above = !cc.causal && kgmin >= qgmax;   // every key at or after every query
+      const bool full = cc.causal ? below : (!alibi || below || above);
+      const int kind = full ? (alibi ? kLinear : kPlain) : kGeneral;
+      cc.q0g = qt.g0;
+      // bias of column col: below: -slope (q0g + col - gj); above: -slope (gj - q0g - col)
+      cc.lin_sl = below ? -slope2 : slope2;
+      cc.lin_base = below ? -slope2 * (float)(qt.g0 - gj) : -slope2 * (float)(gj - qt.g0);
+
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarSFull), i & 1, P.status, kKernBwdTc, kSiteSFull));
+      if (!ok) break;
+      tc::fence_after_sync();
+      float p[64];
+      const float* lse_q = lse_bh + qt.p0 + 64 * h;
+      if (kind == kPlain) compute_p<kPlain>(t_row, h, lse_q, cc, p);
+      else if (kind == kLinear) compute_p<kLinear>(t_row, h, lse_q, cc, p);
+      else compute_p<kGeneral>(t_row, h, lse_q, cc, p);
+      tc::tmem_wait_st();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarPReady));
+
+      // dS^T = P^T o (dP^T - D) into shared memory (bf16, 128-byte swizzle).
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarDPFull), i & 1, P.status, kKernBwdTc, kSiteSFull) &&
+                                       mbar_wait(bar(kBarDSFree), (i & 1) ^ 1, P.status, kKernBwdTc, kSiteBwd));
+      if (!ok) break;
+      tc::fence_after_sync();
+      const float* dv_q = dvec_bh + qt.p0 + 64 * h;
+#pragma unroll
+      for (int ci = 0; ci < 2; ++ci) {
+        uint32_t r[32];
+        tc::tmem_ld32(t_row + kColDP + 64 * h + 32 * ci, r);
+        float4 dvv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) dvv[u] = __ldg(reinterpret_cast<const float4*>(dv_q + 32 * ci) + u);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {  // four 16-byte chunks of 8 columns
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int u = 8 * c8 + 2 * e;
+            const float d0[4] = {dvv[u >> 2].x, dvv[u >> 2].y, dvv[u >> 2].z, dvv[u >> 2].w};
+            const float da = d0[u & 3], db = d0[(u + 1) & 3];
+            const float a = p[32 * ci + u] * (__uint_as_float(r[u]) - da);
+            const float b = p[32 * ci + u + 1] * (__uint_as_float(r[u + 1]) - db);
+            w[e] = tc::pack_bf16(a, b);
+          }
+          const int chunk = 4 * ci + c8;  // 16-byte chunk within the 128-byte row
+          const uint32_t off = (uint32_t)krow * 128u + ((uint32_t)(chunk ^ (krow & 7)) << 4);
+          *reinterpret_cast<uint4*>(ds_tile + off) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      fence_async_smem();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarDSReady));
+
+      // Drain this Q tile's dQ partial (TMEM lane = query row) into the workspace.
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarDQFull), i & 1, P.status, kKernBwdTc, kSiteODone));
+      if (!ok) break;
+      tc::fence_after_sync();
+      float* dq_row = dq_bh + (qt.p0 + krow) * kD + 64 * h;
+#pragma unroll
+      for (int ci = 0; ci < 2; ++ci) {
+        uint32_t r[32];
+        tc::tmem_ld32(t_row + kColDP + 64 * h + 32 * ci, r);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          red_add_v4(dq_row + 32 * ci + 4 * u, __uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
+                     __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarDQEmpty));
+      ++i;
+    }
+    // ------------------------------------------------------------- epilogue: dK (scaled), dV
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarFinal), 0, P.status, kKernBwdTc, kSiteODone));
+    if (ok) {
+      tc::fence_after_sync();
+      // warps 0-3 write dK, warps 4-7 write dV; thread = K/V row, 128 columns.  A
+      // tile that no query sees (none: the walk was empty) gets zero gradients.
+      const uint32_t col0 = h == 0 ? kColDK : kColDV;
+      const float mul = i == 0 ? 0.f : (h == 0 ? P.scale : 1.f);
+      __nv_bfloat16* dst = (h == 0 ? P.dk : P.dv) + (bh * S + kp0 + krow) * kD;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tc::tmem_ld32(t_row + col0 + 32 * c, r);
+        tc::tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          pk[u] = tc::pack_bf16(__uint_as_float(r[2 * u]) * mul, __uint_as_float(r[2 * u + 1]) * mul);
+        uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) d4[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      }
+    }
+    tc::fence_before_sync();
+  }
+
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// dq = scale * dq_acc, fp32 -> bf16, 8 elements per thread.
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc,
+                                                         __nv_bfloat16* __restrict__ dq, float scale,
+                                                         int64_t n8) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
+    const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
+    const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+    uint4 o;
+    o.x = tc::pack_bf16(a.x * scale, a.y * scale);
+    o.y = tc::pack_bf16(a.z * scale, a.w * scale);
+    o.z = tc::pack_bf16(b.x * scale, b.y * scale);
+    o.w = tc::pack_bf16(b.z * scale, b.w * scale);
+    reinterpret_cast<uint4*>(dq)[i] = o;
+  }
+}
+
+}  // namespace
+
+bool bwd_tc_supported(int64_t S, int64_t D, int32_t dtype, const SeqMap& m) {
+  const int64_t chunk = m.layout == RA_LAYOUT_ZIGZAG ? m.h : m.c;
+  return dtype == RA_BF16 && D == kD && S >= kBM && chunk % kBM == 0;
+}
+
+cudaError_t launch_bwd_tc(const AttnArgs& a, const float* lse, const void* dout, const float* dvec,
+                          float* dq_acc, void* dq, void* dk, void* dv, cudaStream_t st) {
+  const int64_t BH = a.B * a.H;
+  if (BH > INT32_MAX) return cudaErrorInvalidValue;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!tc::make_tmap_bhsd(&tq, a.q, BH, a.S, a.D, kBM) || !tc::make_tmap_bhsd(&tk, a.k, BH, a.S, a.D, kBM) ||
+      !tc::make_tmap_bhsd(&tv, a.v, BH, a.S, a.D, kBM) || !tc::make_tmap_bhsd(&tdo, dout, BH, a.S, a.D, kBM))
+    return cudaErrorInvalidValue;
+  BwdParams p;
+  p.map = a.map;
+  p.S = a.S;
+  p.H = (int32_t)a.H;
+  p.BH = (int32_t)BH;
+  p.causal = a.causal;
+  p.slopes = a.slopes;
+  p.c2 = a.scale * kLog2e;
+  p.scale = a.scale;
+  p.lse = lse;
+  p.dvec = dvec;
+  p.dq_acc = dq_acc;
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.status = a.status;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const int64_t tiles = a.S / kBM;
+  const int64_t blocks = tiles * BH;
+  if (blocks > INT32_MAX) return cudaErrorInvalidValue;
+  bwd_tc_kernel<<<(unsigned)blocks, kThreads, kSmemBytes, st>>>(tq, tk, tv, tdo, p);
+  note_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t n8 = BH * a.S * a.D / 8;
+  const int64_t grid = (n8 + 255) / 256 < 152 * 16 ? (n8 + 255) / 256 : 152 * 16;
+  dq_convert_kernel<<<(unsigned)grid, 256, 0, st>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), a.scale, n8);
+  note_launch();
+  return cudaGetLastError();
 }
 
 }  // namespace ra

@@ -30,8 +30,9 @@ cudaError_t launch_permute(const void* x, void* y, int64_t BH, int64_t S, int64_
 
 // ra_simt.cu — CUDA-core kernels (exact fp32 arithmetic)
 cudaError_t launch_fwd_simt(const AttnArgs& a, void* o, float* lse, cudaStream_t st);
+// D_i = dO_i . O_i into dvec; also zeroes dq_acc ([B,H,S,D] fp32) when it is not null.
 cudaError_t launch_bwd_rowdot(const AttnArgs& a, const void* o, const void* dout, float* dvec,
-                              cudaStream_t st);
+                              float* dq_acc, cudaStream_t st);
 cudaError_t launch_bwd_simt(const AttnArgs& a, const float* lse, const void* dout,
                             const float* dvec, void* dq, void* dk, void* dv, cudaStream_t st);
 
@@ -40,7 +41,7 @@ bool fwd_tc_supported(int64_t S, int64_t D, int32_t dtype);
 cudaError_t launch_fwd_tc(const AttnArgs& a, void* o, float* lse, cudaStream_t st);
 
 // ra_bwd_tc.cu — tcgen05 tensor-core backward (bf16, D = 128)
-bool bwd_tc_supported(int64_t S, int64_t D, int32_t dtype);
+bool bwd_tc_supported(int64_t S, int64_t D, int32_t dtype, const SeqMap& m);
 cudaError_t launch_bwd_tc(const AttnArgs& a, const float* lse, const void* dout,
                           const float* dvec, float* dq_acc, void* dq, void* dk, void* dv,
                           cudaStream_t st);

@@ -216,10 +216,15 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(AttnArgs a, T* __res
 template <typename T, int D>
 __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const T* __restrict__ o,
                                                          const T* __restrict__ dout,
-                                                         float* __restrict__ dvec, int64_t rows) {
+                                                         float* __restrict__ dvec,
+                                                         float* __restrict__ dq_acc, int64_t rows) {
   const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
+  if (dq_acc != nullptr) {
+    for (int d = lane * 4; d < D; d += 128)
+      *reinterpret_cast<float4*>(dq_acc + row * D + d) = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   float s = 0.f;
   for (int d = lane * 2; d < D; d += 64) {
     s = fmaf(to_f32<T>(o[row * D + d]), to_f32<T>(dout[row * D + d]), s);
@@ -521,11 +526,12 @@ cudaError_t bwd_simt_t(const AttnArgs& a, const float* lse, const void* dout, co
 }
 
 template <typename T, int D>
-cudaError_t rowdot_t(const AttnArgs& a, const void* o, const void* dout, float* dvec, cudaStream_t st) {
+cudaError_t rowdot_t(const AttnArgs& a, const void* o, const void* dout, float* dvec, float* dq_acc,
+                     cudaStream_t st) {
   const int64_t rows = a.B * a.H * a.S;
   const int64_t blocks = (rows + 7) / 8;
   bwd_rowdot_kernel<T, D><<<(unsigned)blocks, 256, 0, st>>>(static_cast<const T*>(o),
-                                                          static_cast<const T*>(dout), dvec, rows);
+                                                          static_cast<const T*>(dout), dvec, dq_acc, rows);
   note_launch();
   return cudaGetLastError();
 }
@@ -537,9 +543,13 @@ cudaError_t launch_fwd_simt(const AttnArgs& a, void* o, float* lse, cudaStream_t
   return a.D == 64 ? fwd_simt_t<__nv_bfloat16, 64>(a, o, lse, st) : fwd_simt_t<__nv_bfloat16, 128>(a, o, lse, st);
 }
 
-cudaError_t launch_bwd_rowdot(const AttnArgs& a, const void* o, const void* dout, float* dvec, cudaStream_t st) {
-  if (a.dtype == RA_F32) return a.D == 64 ? rowdot_t<float, 64>(a, o, dout, dvec, st) : rowdot_t<float, 128>(a, o, dout, dvec, st);
-  return a.D == 64 ? rowdot_t<__nv_bfloat16, 64>(a, o, dout, dvec, st) : rowdot_t<__nv_bfloat16, 128>(a, o, dout, dvec, st);
+cudaError_t launch_bwd_rowdot(const AttnArgs& a, const void* o, const void* dout, float* dvec, float* dq_acc,
+                              cudaStream_t st) {
+  if (a.dtype == RA_F32)
+    return a.D == 64 ? rowdot_t<float, 64>(a, o, dout, dvec, dq_acc, st)
+                     : rowdot_t<float, 128>(a, o, dout, dvec, dq_acc, st);
+  return a.D == 64 ? rowdot_t<__nv_bfloat16, 64>(a, o, dout, dvec, dq_acc, st)
+                   : rowdot_t<__nv_bfloat16, 128>(a, o, dout, dvec, dq_acc, st);
 }
 
 cudaError_t launch_bwd_simt(const AttnArgs& a, const float* lse, const void* dout, const float* dvec,
