@@ -60,6 +60,11 @@ def lib() -> ctypes.CDLL:
     L.ra_debug_wait_timeout.argtypes = [_i32, _vp]
     L.ra_last_cuda_error.argtypes = []
     L.ra_last_cuda_error.restype = ctypes.c_char_p
+    L.ra_backward_noalloc.argtypes = [_vp] * 9 + [_i64, _i64, _i64, _i64, _i32, _i32, _vp, _f32, _i32,
+                                                    _i32, _vp]
+    L.ra_backward_noalloc.restype = ctypes.c_int32
+    L.ra_noalloc_scratch_bytes.argtypes = []
+    L.ra_noalloc_scratch_bytes.restype = ctypes.c_size_t
     L.ra_kernel_launch_count.argtypes = []
     L.ra_kernel_launch_count.restype = ctypes.c_int64
     for name in ("ra_index_map", "ra_zigzag_permute", "ra_unpermute", "ra_forward", "ra_backward",
@@ -190,3 +195,26 @@ def debug_wait_timeout(limit_us: int, stream=None) -> None:
 def kernel_launch_count() -> int:
     """Kernels the library has launched in this process (host-side counter)."""
     return int(lib().ra_kernel_launch_count())
+
+
+def backward_noalloc(q, k, v, o, lse, dout, *, causal=False, alibi_slopes=None, softmax_scale=None,
+                     N=1, layout="contiguous", out=None, stream=None):
+    """dQ, dK, dV through ra_backward_noalloc: the same backward, for callers that
+    cannot allocate device memory at this point (the library's own fixed scratch
+    buffer replaces the workspace, so problems larger than it are rejected).  The
+    outputs here are allocated by torch unless `out` supplies them."""
+    B, H, S, D = _bhsd(q, "q")
+    for t, n in ((k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
+        if _bhsd(t, n) != q.shape or t.dtype != q.dtype:
+            raise ValueError(f"{n} must match q in shape and dtype")
+    dq, dk, dv = out if out is not None else (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    scale = 0.0 if softmax_scale is None else float(softmax_scale)
+    _check(lib().ra_backward_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                                     _ptr(dk), _ptr(dv), B, H, S, D, DTYPES[q.dtype], int(bool(causal)),
+                                     _ptr(alibi_slopes), scale, N, _layout(layout), _stream(stream)),
+           "ra_backward_noalloc")
+    return dq, dk, dv
+
+
+def noalloc_scratch_bytes() -> int:
+    return int(lib().ra_noalloc_scratch_bytes())

@@ -147,6 +147,35 @@ ra_status ra_backward(const void* q, const void* k, const void* v, const void* o
                       int32_t causal, const float* alibi_slopes, float softmax_scale,
                       int32_t N, ra_layout layout, void* stream);
 
+/*
+ * ra_backward_noalloc — ra_backward for callers that cannot allocate device memory
+ * when they run the backward (e.g. while recording a CUDA graph, inside a host
+ * framework that owns every allocation, or in a loop that cannot afford an
+ * allocation's implicit synchronisation).  The pages have no counterpart to this
+ * call: it only changes where the backward's scratch lives.
+ *   Instead of a caller-provided workspace it uses a fixed scratch buffer inside
+ * the library: RA_NOALLOC_SCRATCH_BYTES (32 MiB) of device memory that every GPU
+ * which loads the library holds until the process exits.  Problems whose
+ * ra_backward_workspace_bytes(B,H,S,D) exceeds that are rejected with
+ * RA_ERR_WORKSPACE before anything is launched (use ra_backward for them).
+ *   All other arguments, layouts, results and errors are those of ra_backward.
+ * The call allocates nothing.  Its first call on a device looks up the buffer's
+ * device address (once per device, with that device current), so make that first
+ * call before any stream capture.  Every call reuses the same buffer: calls that
+ * may overlap on the GPU (different streams without ordering, or several host
+ * threads) race on it and must be serialised by the caller.  The buffer keeps the
+ * last call's contents; each call clears what it needs before using it.
+ */
+#define RA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+ra_status ra_backward_noalloc(const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                              int64_t B, int64_t H, int64_t S, int64_t D, ra_dtype dtype,
+                              int32_t causal, const float* alibi_slopes, float softmax_scale,
+                              int32_t N, ra_layout layout, void* stream);
+
+/* ra_noalloc_scratch_bytes — size of the buffer ra_backward_noalloc uses (bytes). */
+size_t ra_noalloc_scratch_bytes(void);
+
 /* ra_status_string — a static, human-readable name for a status code. */
 const char* ra_status_string(ra_status status);
 
