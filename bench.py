@@ -44,6 +44,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-side-configs", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline time budget")
+    ap.add_argument("--heads", type=int, default=None, help="override H (smaller case of the workload)")
+    ap.add_argument("--seq", type=int, default=None, help="override S (smaller case of the workload)")
     return ap.parse_args()
 
 
@@ -454,8 +456,13 @@ def run_e2e(path, w, args, step_flops, world, max_over_ranks):
 def main():
     args = parse_args()
     sys.path.insert(0, ROOT)
+    import dataclasses
+
     from context_ra_forward_gb300 import inputs
     w = inputs.WORKLOADS[args.workload]
+    if args.heads or args.seq:
+        w = dataclasses.replace(w, H=args.heads or w.H, S=args.seq or w.S,
+                                name=f"{w.name}-small(H={args.heads or w.H},S={args.seq or w.S})")
     if args.impl == "reference":
         run_reference(args, w)
     else:

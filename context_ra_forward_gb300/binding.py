@@ -58,6 +58,8 @@ def lib() -> ctypes.CDLL:
     L.ra_check_device_status.argtypes = [_vp, _vp]
     L.ra_forward_path.argtypes = [_i64, _i64, _i64, _i64, _i32, _i32, _i32]
     L.ra_debug_wait_timeout.argtypes = [_i32, _vp]
+    L.ra_debug_wait_sites.argtypes = [_vp, _i32]
+    L.ra_debug_wait_sites.restype = ctypes.c_int32
     L.ra_last_cuda_error.argtypes = []
     L.ra_last_cuda_error.restype = ctypes.c_char_p
     L.ra_backward_noalloc.argtypes = [_vp] * 9 + [_i64, _i64, _i64, _i64, _i32, _i32, _vp, _f32, _i32,
@@ -218,3 +220,12 @@ def backward_noalloc(q, k, v, o, lse, dout, *, causal=False, alibi_slopes=None, 
 
 def noalloc_scratch_bytes() -> int:
     return int(lib().ra_noalloc_scratch_bytes())
+
+
+def debug_wait_sites():
+    """Per warp of the first failing block: (site, parity, barrier address low bits)
+    of the wait that gave up, or None for warps that did not give up."""
+    n = lib().ra_debug_wait_sites(None, 0)
+    buf = (ctypes.c_int32 * n)()
+    lib().ra_debug_wait_sites(ctypes.cast(buf, ctypes.c_void_p), n)
+    return [None if v == 0 else ((v >> 24) & 0xff, (v >> 16) & 1, v & 0xffff) for v in buf]

@@ -15,7 +15,7 @@
 
 namespace {
 
-__device__ int32_t g_status_word[4];
+__device__ int32_t g_status_word[ra::kStatusWords];
 
 constexpr int kMaxDevices = 64;
 int32_t* g_status_ptr[kMaxDevices] = {};
@@ -113,6 +113,7 @@ ra_status attn_args(const void* q, const void* k, const void* v, int64_t B, int6
 }
 
 std::atomic<int64_t> g_launches{0};
+int32_t g_last_sites[ra::kStatusWarps] = {};
 
 }  // namespace
 
@@ -248,15 +249,22 @@ ra_status ra_check_device_status(void* stream, int32_t* detail_host) {
   if (status_word(&word) != RA_OK) return RA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(st) != cudaSuccess) return RA_ERR_CUDA;
-  int32_t h[4] = {0, 0, 0, 0};
+  int32_t h[ra::kStatusWords] = {};
   if (cudaMemcpy(h, word, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return RA_ERR_CUDA;
   if (h[0] != 0) {
-    const int32_t zero[4] = {0, 0, 0, 0};
+    memcpy(g_last_sites, h + 4, sizeof(g_last_sites));
+    const int32_t zero[ra::kStatusWords] = {};
     if (cudaMemcpy(word, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return RA_ERR_CUDA;
   }
-  if (detail_host) memcpy(detail_host, h, sizeof(h));
+  if (detail_host) memcpy(detail_host, h, 4 * sizeof(int32_t));
   if (h[0] == RA_ERR_TIMEOUT) return RA_ERR_TIMEOUT;
   return h[0] == 0 ? RA_OK : RA_ERR_CUDA;
+}
+
+int32_t ra_debug_wait_sites(int32_t* host, int32_t n) {
+  const int32_t m = n < ra::kStatusWarps ? n : ra::kStatusWarps;
+  if (host) memcpy(host, g_last_sites, (size_t)(m > 0 ? m : 0) * sizeof(int32_t));
+  return ra::kStatusWarps;
 }
 
 ra_status ra_debug_wait_timeout(int32_t limit_us, void* stream) {

@@ -17,7 +17,8 @@
 // Warp roles (320 threads):
 //   warps 0-7  "softmax": warp w owns K/V rows 32*(w%4).. (its TMEM lane quarter)
 //              and Q columns 64*(w/4)..: P^T, dS^T, the dQ drain, the dK/dV epilogue
-//   warp  8    TMA producer: K and V once, then Q and dO tiles into a 2-stage ring
+//   warp  8    TMA producer: K and V once, then Q and dO tiles into a 2-stage ring;
+//              it also issues the bulk reduce-add of each Q tile's dQ partial
 //   warp  9    TMEM allocation and MMA issue (one thread)
 // TMEM (512 columns): S^T [0,128), dP^T [128,256), dK [256,384), dV [384,512);
 // all fp32 with K/V row r in lane r.  P^T (bf16 pairs) is written back over S^T
@@ -28,8 +29,9 @@
 //
 // MMA order per Q tile i:  [P^T_i] dV_i  [dS^T_i] dK_i, dQ_i -> S^T_{i+1}
 //                          [dQ_i drained] dP^T_{i+1}.
-// dQ partials are added into an fp32 workspace (zeroed by the row-term pre-pass)
-// with 16-byte atomic adds; a post-pass scales and converts them.
+// dQ partials are staged in shared memory and added into an fp32 workspace
+// (zeroed by the row-term pre-pass) with TMA reduce-adds (four boxes per Q tile),
+// issued by the TMA warp; a post-pass scales and converts them.
 #include <cuda.h>
 #include <math.h>
 #include <mutex>
@@ -62,8 +64,8 @@ constexpr uint32_t kOffBar = kOffDS + kTileBytes;
 enum Bar {
   kBarKV = 0,
   kBarQFull = 1,  // + stage
-  kBarQEmpty = 3, // + stage
-  kBarSFull = 5,
+  kBarDrainFull = 3,  // the dQ partial of a Q tile is staged in its Q/dO stage
+  kBarSFull = 4,
   kBarDPFull,
   kBarPReady,
   kBarDSReady,
@@ -127,7 +129,11 @@ struct QWalk {
     while (ti >= tend) {
       if (++seg >= nseg) {
         seg = 0;
-        if (++t >= m.N) return false;
+        if (++t >= m.N) {
+          t = m.N;  // exhausted: every later call returns false too
+          seg = nseg;
+          return false;
+        }
       }
       const int32_t s = (s0 + t) % m.N;  // step t: the queries of shard (s0 + t) mod N
       int64_t len;
@@ -211,15 +217,10 @@ __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  const __grid_constant__ BwdParams P) {
+                  const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ BwdParams P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -244,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t cnt = 1;
-      if (i == kBarPReady || i == kBarDSReady || i == kBarDQEmpty) cnt = 8;
+      if (i == kBarPReady || i == kBarDSReady || i == kBarDQEmpty || i == kBarDrainFull) cnt = 8;
       mbar_init(bar(i), cnt);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -264,32 +265,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tma_prefetch_desc(&tm_k);
       tc::tma_prefetch_desc(&tm_v);
       tc::tma_prefetch_desc(&tm_do);
+      tc::tma_prefetch_desc(&tm_dq);
       const int32_t z = (int32_t)bh;
       mbar_arrive_expect_tx(bar(kBarKV), 2 * kTileBytes);
       for (int hf = 0; hf < 2; ++hf) {
         tc::tma_load_3d(sbase + kOffK + hf * kBoxBytes, &tm_k, hf * 64, (int32_t)kp0, z, bar(kBarKV));
         tc::tma_load_3d(sbase + kOffV + hf * kBoxBytes, &tm_v, hf * 64, (int32_t)kp0, z, bar(kBarKV));
       }
+      // Stage s holds Q and dO of Q tile i (s = i & 1) and, once that tile's MMAs
+      // are done, its dQ partial: after the softmax warps have staged it, this warp
+      // adds it to the accumulator with one bulk reduce, then refills the stage.
       QWalk walk;
       walk.init(&P, kg0, s0);
       QTile qt;
-      int i = 0;
-      while (walk.next(qt)) {
-        const int st = i & 1;
-        if (!mbar_wait(bar(kBarQEmpty + st), ((i >> 1) & 1) ^ 1, P.status, kKernBwdTc, kSiteKEmpty)) break;
-        mbar_arrive_expect_tx(bar(kBarQFull + st), kStageBytes);
+      int64_t stage_p0[2] = {0, 0};
+      int loaded = 0;
+      auto load = [&](const QTile& t) {
+        const int st = loaded & 1;
         const uint32_t dst = sbase + kOffQ + st * kStageBytes;
+        mbar_arrive_expect_tx(bar(kBarQFull + st), kStageBytes);
         for (int hf = 0; hf < 2; ++hf) {
-          tc::tma_load_3d(dst + hf * kBoxBytes, &tm_q, hf * 64, (int32_t)qt.p0, z, bar(kBarQFull + st));
-          tc::tma_load_3d(dst + kTileBytes + hf * kBoxBytes, &tm_do, hf * 64, (int32_t)qt.p0, z,
+          tc::tma_load_3d(dst + hf * kBoxBytes, &tm_q, hf * 64, (int32_t)t.p0, z, bar(kBarQFull + st));
+          tc::tma_load_3d(dst + kTileBytes + hf * kBoxBytes, &tm_do, hf * 64, (int32_t)t.p0, z,
                           bar(kBarQFull + st));
         }
-        ++i;
+        stage_p0[st] = t.p0;
+        ++loaded;
+      };
+      for (int s = 0; s < 2 && walk.next(qt); ++s) load(qt);
+      for (int i = 0; i < loaded; ++i) {
+        const int st = i & 1;
+        if (!mbar_wait(bar(kBarDrainFull), i & 1, P.status, kKernBwdTc, kSiteBwd)) break;
+        for (int b = 0; b < 4; ++b)  // four 128-row x 32-column fp32 boxes
+          tc::tma_reduce_add_3d(&tm_dq, sbase + kOffQ + st * kStageBytes + b * kBoxBytes, 32 * b,
+                                (int32_t)stage_p0[st], z);
+        tc::bulk_commit();
+        tc::bulk_wait_read0();  // the stage may be overwritten from here on
+        if (walk.next(qt)) load(qt);
       }
+      tc::bulk_wait_all0();
       // Let every load this warp issued land before the CTA can exit.
       mbar_wait(bar(kBarKV), 0, P.status, kKernBwdTc, kSiteKFull);
-      for (int back = 1; back <= 2 && back <= i; ++back) {
-        const int ii = i - back;
+      for (int back = 1; back <= 2 && back <= loaded; ++back) {
+        const int ii = loaded - back;
         mbar_wait(bar(kBarQFull + (ii & 1)), (ii >> 1) & 1, P.status, kKernBwdTc, kSiteQFull);
       }
     }
@@ -351,7 +369,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::mma_commit(bar(kBarDSFree));
         tc::mma_commit(bar(kBarDQFull));
-        tc::mma_commit(bar(kBarQEmpty + st));
         more = walk.next(qt);
         if (!more) break;
         const int nst = (i + 1) & 1;
@@ -402,7 +419,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* ds_tile = sgen + kOffDS + h * kBoxBytes;
     const float* lse_bh = P.lse + bh * S;
     const float* dvec_bh = P.dvec + bh * S;
-    float* dq_bh = P.dq_acc + bh * S * kD;
 
     QWalk walk;
     walk.init(&P, kg0, s0);
@@ -471,24 +487,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarDSReady));
 
-      // Drain this Q tile's dQ partial (TMEM lane = query row) into the workspace.
+      // Drain this Q tile's dQ partial (TMEM lane = query row): into registers, free
+      // the TMEM region, then stage it in the tile's Q/dO stage, which the tile's
+      // finished MMAs no longer need, for the TMA warp's reduce-add.
       ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarDQFull), i & 1, P.status, kKernBwdTc, kSiteODone));
       if (!ok) break;
       tc::fence_after_sync();
-      float* dq_row = dq_bh + (qt.p0 + krow) * kD + 64 * h;
-#pragma unroll
-      for (int ci = 0; ci < 2; ++ci) {
-        uint32_t r[32];
-        tc::tmem_ld32(t_row + kColDP + 64 * h + 32 * ci, r);
+      {
+        uint32_t r0[32], r1[32];
+        tc::tmem_ld32(t_row + kColDP + 64 * h, r0);
+        tc::tmem_ld32(t_row + kColDP + 64 * h + 32, r1);
         tc::tmem_wait_ld();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarDQEmpty));
+        // fp32 boxes of 128 rows x 32 columns (128-byte rows, 128-byte swizzle):
+        // this warp's columns 64h..64h+63 are boxes 2h and 2h+1.
+        uint8_t* box0 = sgen + kOffQ + (i & 1) * kStageBytes + (2 * h) * kBoxBytes + krow * 128;
+        uint8_t* box1 = box0 + kBoxBytes;
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          red_add_v4(dq_row + 32 * ci + 4 * u, __uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
-                     __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t off = (uint32_t)((c ^ (krow & 7)) << 4);
+          *reinterpret_cast<uint4*>(box0 + off) = make_uint4(r0[4 * c], r0[4 * c + 1], r0[4 * c + 2], r0[4 * c + 3]);
+          *reinterpret_cast<uint4*>(box1 + off) = make_uint4(r1[4 * c], r1[4 * c + 1], r1[4 * c + 2], r1[4 * c + 3]);
+        }
       }
-      tc::fence_before_sync();
+      fence_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarDQEmpty));
+      if (lane == 0) mbar_arrive(bar(kBarDrainFull));
       ++i;
     }
     // ------------------------------------------------------------- epilogue: dK (scaled), dV
@@ -551,9 +577,10 @@ cudaError_t launch_bwd_tc(const AttnArgs& a, const float* lse, const void* dout,
                           float* dq_acc, void* dq, void* dk, void* dv, cudaStream_t st) {
   const int64_t BH = a.B * a.H;
   if (BH > INT32_MAX) return cudaErrorInvalidValue;
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq;
   if (!tc::make_tmap_bhsd(&tq, a.q, BH, a.S, a.D, kBM) || !tc::make_tmap_bhsd(&tk, a.k, BH, a.S, a.D, kBM) ||
-      !tc::make_tmap_bhsd(&tv, a.v, BH, a.S, a.D, kBM) || !tc::make_tmap_bhsd(&tdo, dout, BH, a.S, a.D, kBM))
+      !tc::make_tmap_bhsd(&tv, a.v, BH, a.S, a.D, kBM) || !tc::make_tmap_bhsd(&tdo, dout, BH, a.S, a.D, kBM) ||
+      !tc::make_tmap_bhsd_f32(&tdq, dq_acc, BH, a.S, a.D, kBM))
     return cudaErrorInvalidValue;
   BwdParams p;
   p.map = a.map;
@@ -579,7 +606,7 @@ cudaError_t launch_bwd_tc(const AttnArgs& a, const float* lse, const void* dout,
   const int64_t tiles = a.S / kBM;
   const int64_t blocks = tiles * BH;
   if (blocks > INT32_MAX) return cudaErrorInvalidValue;
-  bwd_tc_kernel<<<(unsigned)blocks, kThreads, kSmemBytes, st>>>(tq, tk, tv, tdo, p);
+  bwd_tc_kernel<<<(unsigned)blocks, kThreads, kSmemBytes, st>>>(tq, tk, tv, tdo, tdq, p);
   note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

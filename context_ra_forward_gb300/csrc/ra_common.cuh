@@ -11,7 +11,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
-#include "../../include/ra.h"
+#include "ra.h"
 
 namespace ra {
 
@@ -91,7 +91,12 @@ struct SeqMap {
 // ----------------------------------------------------------------------------
 // Status word: [0] code, [1] kernel id, [2] block, [3] wait site.  The first
 // failure wins; the host reads and clears it in ra_check_device_status.
+// Words [4, 4 + kStatusWarps) record, for the block that failed first, what each
+// warp was waiting on when its wait gave up: site << 24 | parity << 16 | the low
+// 16 bits of the barrier's shared address (0 = that warp did not give up).
 // ----------------------------------------------------------------------------
+constexpr int kStatusWarps = 32;
+constexpr int kStatusWords = 4 + kStatusWarps;
 __device__ __forceinline__ void record_failure(int32_t* status, int32_t code, int32_t kernel,
                                                int32_t site) {
   if (status == nullptr) return;
@@ -144,6 +149,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // A wait also gives up as soon as the status word holds a failure, so one lost
 // signal ends the whole launch quickly; the word stays set (and later waits keep
 // giving up) until the host reads and clears it.
+__device__ __forceinline__ void record_wait_site(int32_t* status, uint32_t bar, uint32_t parity, int32_t site) {
+  if (status == nullptr) return;
+  const int32_t me = (int32_t)(blockIdx.x + gridDim.x * blockIdx.y);
+  const int w = (int)(threadIdx.x >> 5);
+  if (*reinterpret_cast<volatile int32_t*>(status + 2) == me && w < kStatusWarps)
+    status[4 + w] = (site << 24) | (int32_t)((parity & 1u) << 16) | (int32_t)(bar & 0xffffu);
+}
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* status,
                                           int32_t kernel, int32_t site,
                                           uint64_t limit_ns = kWaitLimitNs) {
@@ -153,9 +165,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (status != nullptr && *reinterpret_cast<volatile int32_t*>(status) != 0) return false;
+    if (status != nullptr && *reinterpret_cast<volatile int32_t*>(status) != 0) {
+      record_wait_site(status, bar, parity, site);
+      return false;
+    }
     if (globaltimer_ns() - t0 > limit_ns) {
       record_failure(status, RA_ERR_TIMEOUT, kernel, site);
+      record_wait_site(status, bar, parity, site);
       return false;
     }
   }

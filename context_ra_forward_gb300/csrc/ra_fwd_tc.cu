@@ -131,7 +131,11 @@ struct KvWalk {
       while (ti >= tend) {
         if (++seg >= nseg) {
           seg = 0;
-          if (++t >= m.N) return false;
+          if (++t >= m.N) {
+            t = m.N;  // exhausted: every later call returns false too
+            seg = nseg;
+            return false;
+          }
         }
         const int32_t s = (r0 - t + m.N) % m.N;  // ring step t meets shard (r0 - t) mod N
         int64_t len;

@@ -53,6 +53,23 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int3
       : "memory");
 }
 
+// TMA reduce-add of one shared-memory box into the global tensor of `tmap` at the
+// given coordinates (element type and swizzle as the map says), tracked by bulk groups.
+__device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, uint32_t src, int32_t c0, int32_t c1,
+                                                  int32_t c2) {
+  asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                   tmap),
+               "r"(c0), "r"(c1), "r"(c2), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until every committed bulk group has finished reading its shared source.
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Waits until every committed bulk group has completed.
+__device__ __forceinline__ void bulk_wait_all0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // ---------------------------------------------------------------- TMEM
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
@@ -138,6 +155,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // A [BH, S, D] bf16 tensor as a 3-D TMA map with a 64 x box_rows x 1 box and
 // 128-byte swizzle; rows past S read as zero.
 bool make_tmap_bhsd(CUtensorMap* map, const void* base, int64_t BH, int64_t S, int64_t D, int box_rows);
+// The same for an fp32 [BH, S, D] tensor with a 32 x box_rows x 1 box (128-byte rows).
+bool make_tmap_bhsd_f32(CUtensorMap* map, const void* base, int64_t BH, int64_t S, int64_t D, int box_rows);
 
 }  // namespace tc
 }  // namespace ra

@@ -199,6 +199,15 @@ int32_t ra_forward_path(int64_t B, int64_t H, int64_t S, int64_t D, ra_dtype dty
                         int32_t N, ra_layout layout);
 
 /*
+ * ra_debug_wait_sites — after ra_check_device_status reported a failure: for the
+ * block that failed first, what each of its warps was waiting on when its wait
+ * gave up, one int32 per warp (site << 24 | parity << 16 | low 16 bits of the
+ * barrier's shared-memory address; 0 = the warp did not give up).  Copies up to n
+ * entries to `host` (may be NULL) and returns how many entries exist.  Host only.
+ */
+int32_t ra_debug_wait_sites(int32_t* host, int32_t n);
+
+/*
  * ra_debug_wait_timeout — failure-detection self test.  Launches one block whose
  * warp waits on an mbarrier that nothing ever arrives on, with a limit of
  * `limit_us` microseconds; the wait gives up, records RA_ERR_TIMEOUT in the device
