@@ -72,19 +72,25 @@ def source_hash(files):
 
 
 def committed_traffic(kernel):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the kernel source as it is now (else None)."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes per launch from the committed ncu summary (profiles/traffic.txt:
+    `kernel bytes source_hash source,...`), if it was taken on the kernel source as
+    it is now (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
     try:
         with open(path) as f:
-            rec = json.load(f).get(kernel)
-    except (OSError, ValueError):
+            lines = [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+    except OSError:
         return None
-    if not rec:
-        return None
-    if rec.get("source_hash") != source_hash(rec.get("sources", [])):
-        return None
-    return rec
+    for parts in lines:
+        if len(parts) == 4 and parts[0] == kernel:
+            sources = parts[3].split(",")
+            try:
+                if source_hash(sources) != parts[2]:
+                    return None
+            except OSError:
+                return None
+            return {"dram_bytes_per_launch": int(parts[1])}
+    return None
 
 
 class ClockSampler:

@@ -172,12 +172,15 @@ struct ColCtx {
   bool causal, alibi;
 };
 
+// col: query column within the tile; colh: the same within this warp's 64-column
+// half (a compile-time constant in the unrolled loops; the half's offset is folded
+// into lin_base, so the ALiBi term needs no per-element int -> float conversion).
 template <int kKind>
-__device__ __forceinline__ float prob(float s, float lse2, int col, const ColCtx& c) {
+__device__ __forceinline__ float prob(float s, float lse2, int col, int colh, const ColCtx& c) {
   if constexpr (kKind == kPlain) {
     return tc::ex2(fmaf(s, c.c2, -lse2));
   } else if constexpr (kKind == kLinear) {
-    return tc::ex2(fmaf(s, c.c2, fmaf(c.lin_sl, (float)col, c.lin_base) - lse2));
+    return tc::ex2(fmaf(s, c.c2, fmaf(c.lin_sl, (float)colh, c.lin_base) - lse2));
   } else {
     const int64_t gi = c.q0g + col;
     const bool vis = !c.causal || c.gj <= gi;
@@ -204,7 +207,7 @@ __device__ __forceinline__ void compute_p(uint32_t t_row, int h, const float* ls
     for (int u = 0; u < 32; ++u) {
       const float l4[4] = {lv[u >> 2].x, lv[u >> 2].y, lv[u >> 2].z, lv[u >> 2].w};
       const float lse2 = l4[u & 3] * kLog2e;
-      p[32 * ci + u] = prob<kKind>(__uint_as_float(r[u]), lse2, 64 * h + 32 * ci + u, c);
+      p[32 * ci + u] = prob<kKind>(__uint_as_float(r[u]), lse2, 64 * h + 32 * ci + u, 32 * ci + u, c);
     }
   }
   uint32_t pk[32];
@@ -232,11 +235,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const SeqMap& m = P.map;
   const int64_t S = P.S;
 
-  // Work item: K/V tile (lowest global positions first under causal: they are
-  // seen by the most queries) and (b, h).
+  // Work item: (b, h) major, then the K/V tile (lowest global positions first
+  // under causal: they are seen by the most queries).  Resident CTAs then belong
+  // to one or two heads and share that head's Q/dO tiles and dQ rows in L2 (with
+  // heads minor they spanned every head and the kernel ran at the DRAM roofline).
   const int64_t L = blockIdx.x;
-  const int64_t tile = L / P.BH;
-  const int64_t bh = L - tile * P.BH;
+  const int64_t ntiles = S / kBM;
+  const int64_t bh = L / ntiles;
+  const int64_t tile = L - bh * ntiles;
   const int hh = (int)(bh % P.H);
   const int64_t kp0 = P.causal ? m.inv(tile * kBM) : tile * kBM;
   const int64_t kg0 = m.g(kp0);
@@ -436,7 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       cc.q0g = qt.g0;
       // bias of column col: below: -slope (q0g + col - gj); above: -slope (gj - q0g - col)
       cc.lin_sl = below ? -slope2 : slope2;
-      cc.lin_base = below ? -slope2 * (float)(qt.g0 - gj) : -slope2 * (float)(gj - qt.g0);
+      cc.lin_base = (below ? -slope2 * (float)(qt.g0 - gj) : -slope2 * (float)(gj - qt.g0)) +
+                    cc.lin_sl * (float)(64 * h);  // this warp's first column
 
       ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarSFull), i & 1, P.status, kKernBwdTc, kSiteSFull));
       if (!ok) break;

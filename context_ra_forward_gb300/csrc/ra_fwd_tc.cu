@@ -204,12 +204,13 @@ enum TileKind { kPlain = 0, kLinear = 1, kGeneral = 2 };
 // Score of column u in the log2 domain.  kPlain keeps the raw score (scaled
 // inside the exponent); kLinear adds the ALiBi bias of a tile that lies wholly
 // on one side of every query; kGeneral masks and biases element by element.
+// `lin` is the ALiBi term of this column for kLinear (c.base + c.sl * u), else unused.
 template <int kKind>
-__device__ __forceinline__ float tile_score(int u, float raw, const RowCtx& c) {
+__device__ __forceinline__ float tile_score(int u, float raw, float lin, const RowCtx& c) {
   if constexpr (kKind == kPlain) {
     return raw;
   } else if constexpr (kKind == kLinear) {
-    return fmaf(raw, c.c2, fmaf(c.sl, (float)u, c.base));
+    return fmaf(raw, c.c2, lin);
   } else {
     const int64_t gj = c.contig ? c.gk0 + u : (int64_t)c.gtab[u];
     const bool vis = c.row_ok && u < c.valid && (!c.causal || gj <= c.gi);
@@ -226,9 +227,13 @@ __device__ __forceinline__ float tile_max(uint32_t t_s, const RowCtx& c) {
   for (int ch = 0; ch < 4; ++ch) {
     uint32_t r[32];
     tc::tmem_ld32(t_s + 32 * ch, r);
+    // ALiBi term of column 32ch + u is lb + sl*u: the chunk's part once, the
+    // column's part an immediate (no per-element int -> float conversion)
+    const float lb = fmaf(c.sl, (float)(32 * ch), c.base);
     tc::tmem_wait_ld();
 #pragma unroll
-    for (int u = 0; u < 32; ++u) mx[u & 3] = fmaxf(mx[u & 3], tile_score<kKind>(32 * ch + u, __uint_as_float(r[u]), c));
+    for (int u = 0; u < 32; ++u)
+      mx[u & 3] = fmaxf(mx[u & 3], tile_score<kKind>(32 * ch + u, __uint_as_float(r[u]), fmaf(c.sl, (float)u, lb), c));
   }
   const float m = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
   return kKind == kPlain ? m * c.c2 : m;
@@ -240,6 +245,7 @@ __device__ __forceinline__ float tile_probs(uint32_t t_s, float mu, const RowCtx
 #pragma unroll 1
   for (int hf = 0; hf < 2; ++hf) {
     uint32_t pk[32];
+    const float lb = fmaf(c.sl, (float)(64 * hf), c.base);
 #pragma unroll
     for (int ci = 0; ci < 2; ++ci) {
       uint32_t r[32];
@@ -248,8 +254,10 @@ __device__ __forceinline__ float tile_probs(uint32_t t_s, float mu, const RowCtx
 #pragma unroll
       for (int u = 0; u < 16; ++u) {
         const int col = 64 * hf + 32 * ci + 2 * u;
-        const float a = tile_score<kKind>(col, __uint_as_float(r[2 * u]), c);
-        const float b = tile_score<kKind>(col + 1, __uint_as_float(r[2 * u + 1]), c);
+        const float la = fmaf(c.sl, (float)(32 * ci + 2 * u), lb);
+        const float lb1 = fmaf(c.sl, (float)(32 * ci + 2 * u + 1), lb);
+        const float a = tile_score<kKind>(col, __uint_as_float(r[2 * u]), la, c);
+        const float b = tile_score<kKind>(col + 1, __uint_as_float(r[2 * u + 1]), lb1, c);
         float pa, pb;
         if constexpr (kKind == kPlain) {
           pa = tc::ex2(fmaf(a, c.c2, -mu));
@@ -304,10 +312,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const SeqMap& m = P.map;
   const int64_t S = P.S;
 
-  // Work item: pair index (heaviest first when causal and aligned) and (b, h).
+  // Work item: (b, h) major, then the pair index (heaviest first when causal and
+  // aligned).  Resident CTAs then belong to one or two heads and share that
+  // head's K/V tiles in L2 (with heads minor, the resident CTAs spanned every head,
+  // whose tensors sit at power-of-two strides, and nearly every K/V tile load
+  // went to DRAM).
   const int64_t L = blockIdx.x;
-  const int64_t pair = L / P.BH;
-  const int64_t bh = L - pair * P.BH;
+  const int64_t npairs = (S + 255) / 256;
+  const int64_t bh = L / npairs;
+  const int64_t pair = L - bh * npairs;
   const int hh = (int)(bh % P.H);
   const int64_t P0 = P.heavy_first ? m.inv(S - 256 * (pair + 1)) : 256 * pair;
   const int64_t qend = P0 + 256 < S ? P0 + 256 : S;
