@@ -24,8 +24,9 @@
 // all fp32 with K/V row r in lane r.  P^T (bf16 pairs) is written back over S^T
 // (Q columns 0..63 -> TMEM columns 0..31, 64..127 -> 64..95), the dQ partial of
 // a Q tile (row = query) goes into the dP^T region once that has been read.
-// dS^T (bf16) goes to shared memory in the 128-byte-swizzled layout, where it is
-// the K-major A operand of dK += dS^T Q and the MN-major A operand of dQ = dS K.
+// dS^T (bf16) is written back over dP^T in TMEM (same column map as P^T), the A
+// operand of dK += dS^T Q, and to shared memory in the 128-byte-swizzled layout,
+// the MN-major A operand of dQ = dS K.
 //
 // MMA order per Q tile i:  [P^T_i] dV_i  [dS^T_i] dK_i, dQ_i -> S^T_{i+1}
 //                          [dQ_i drained] dP^T_{i+1}.
@@ -363,10 +364,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc::fence_after_sync();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // dK += dS^T Q   (A K-major, B MN-major)
-          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-          tc::mma_ss(tmem + kColDK, tc::smem_desc(dsb + off, 16, 1024),
-                     tc::smem_desc(qb + kk * 2048, kBoxBytes, 1024), kIdescKM, (i > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 8; ++kk) {  // dK += dS^T Q   (A = dS^T from TMEM, B MN-major)
+          const uint32_t acol = kColDP + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+          tc::mma_ts(tmem + kColDK, tmem + acol, tc::smem_desc(qb + kk * 2048, kBoxBytes, 1024), kIdescKM,
+                     (i > 0 || kk > 0) ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {  // dQ_i = dS K   (A = dS^T MN-major, B = K MN-major)
@@ -464,6 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc::fence_after_sync();
       const float* dv_q = dvec_bh + qt.p0 + 64 * h;
+      uint32_t dsk[32];  // dS^T as bf16 pairs, for the dK product from TMEM
 #pragma unroll
       for (int ci = 0; ci < 2; ++ci) {
         uint32_t r[32];
@@ -483,12 +485,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float a = p[32 * ci + u] * (__uint_as_float(r[u]) - da);
             const float b = p[32 * ci + u + 1] * (__uint_as_float(r[u + 1]) - db);
             w[e] = tc::pack_bf16(a, b);
+            dsk[16 * ci + 4 * c8 + e] = w[e];
           }
           const int chunk = 4 * ci + c8;  // 16-byte chunk within the 128-byte row
           const uint32_t off = (uint32_t)krow * 128u + ((uint32_t)(chunk ^ (krow & 7)) << 4);
           *reinterpret_cast<uint4*>(ds_tile + off) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
+      // dS^T pairs over this warp's dP^T columns (all read above): query columns
+      // 64h..64h+63 -> TMEM columns kColDP + 64h .. + 31.
+      tc::tmem_st32(t_row + kColDP + 64 * h, dsk);
+      tc::tmem_wait_st();
       fence_async_smem();
       tc::fence_before_sync();
       __syncwarp();
