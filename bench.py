@@ -39,7 +39,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="C5", choices=["C2", "C3", "C4", "C5"])
+    ap.add_argument("--workload", default="C5", choices=["C2", "C3", "C4", "C5", "C3S", "C5S"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-side-configs", action="store_true")
@@ -400,7 +400,7 @@ def run_ours(args, w):
 
     side = {}
     if not args.no_side_configs and rank == 0:
-        for c in ("C2", "C3", "C4"):
+        for c in ("C2", "C3", "C4", "C3S"):
             if c != w.name:
                 side[c] = side_config(c, dev)
 

@@ -21,7 +21,7 @@ STATUS_NAMES = {0: "RA_OK", -1: "RA_ERR_INVALID_ARG", -2: "RA_ERR_UNSUPPORTED",
                 -3: "RA_ERR_MISALIGNED", -4: "RA_ERR_CUDA", -5: "RA_ERR_TIMEOUT",
                 -6: "RA_ERR_WORKSPACE"}
 DTYPES = {torch.float32: 0, torch.bfloat16: 1}
-LAYOUTS = {"contiguous": 0, "zigzag": 1}
+LAYOUTS = {"contiguous": 0, "zigzag": 1, "strided": 2}
 
 
 class RAError(RuntimeError):

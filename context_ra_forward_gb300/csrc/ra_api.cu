@@ -44,7 +44,8 @@ ra_status check_sizes(int64_t B, int64_t H, int64_t S, int64_t D, ra_dtype dt, i
                       ra_layout layout) {
   if (B < 0 || H < 0 || S < 0) return RA_ERR_INVALID_ARG;
   if (dt != RA_F32 && dt != RA_BF16) return RA_ERR_UNSUPPORTED;
-  if (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_ZIGZAG) return RA_ERR_UNSUPPORTED;
+  if (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_ZIGZAG && layout != RA_LAYOUT_STRIDED)
+    return RA_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return RA_ERR_UNSUPPORTED;
   if (N < 1) return RA_ERR_INVALID_ARG;
   const int64_t parts = layout == RA_LAYOUT_ZIGZAG ? 2 * (int64_t)N : (int64_t)N;
@@ -144,7 +145,8 @@ const char* ra_status_string(ra_status s) {
 }
 
 ra_status ra_index_map(int64_t S, int32_t N, ra_layout layout, int64_t* perm_host, int64_t* inv_host) {
-  if (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_ZIGZAG) return RA_ERR_UNSUPPORTED;
+  if (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_ZIGZAG && layout != RA_LAYOUT_STRIDED)
+    return RA_ERR_UNSUPPORTED;
   if (S < 0 || N < 1) return RA_ERR_INVALID_ARG;
   const int64_t parts = layout == RA_LAYOUT_ZIGZAG ? 2 * (int64_t)N : (int64_t)N;
   if (S % parts) return RA_ERR_INVALID_ARG;

@@ -108,7 +108,8 @@ struct QTile {
 };
 
 // Q tiles that see a K/V tile, in ring order; every 128-row tile lies inside one
-// chunk (chunk length a multiple of 128), so each is a contiguous global range.
+// run (a zig-zag chunk, or a shard otherwise, a multiple of 128 slots long), so
+// its global positions are g0, g0 + step, ... (step 1, or N when strided).
 struct QWalk {
   const BwdParams* P;
   int64_t kgmin;
@@ -145,20 +146,23 @@ struct QWalk {
       } else {
         len = m.c;
         seg_p0 = s * m.c;
-        seg_g0 = seg_p0;
+        seg_g0 = m.g(seg_p0);  // s for strided, s*c for contiguous
       }
+      const int64_t step = m.run_step();
       tend = len / kBM;
       ti = 0;
       if (P->causal) {
-        if (seg_g0 + len - 1 < kgmin) {
+        // tile ti covers seg_g0 + 128*step*ti .. + 127*step; it is visible if its
+        // last query is not before the K/V tile's first key
+        if (seg_g0 + (len - 1) * step < kgmin) {
           tend = 0;
-        } else if (kgmin > seg_g0) {
-          ti = (kgmin - seg_g0) / kBM;
+        } else if (kgmin > seg_g0 + (kBM - 1) * step) {
+          ti = (kgmin - seg_g0 - (kBM - 1) * step + kBM * step - 1) / (kBM * step);
         }
       }
     }
     out.p0 = seg_p0 + ti * kBM;
-    out.g0 = seg_g0 + ti * kBM;
+    out.g0 = seg_g0 + ti * kBM * P->map.run_step();
     ++ti;
     return true;
   }
@@ -166,10 +170,11 @@ struct QWalk {
 
 enum TileKind { kPlain = 0, kLinear = 1, kGeneral = 2 };
 
-// Probability P^T of K/V row gj against query column (q0g + col), log2 domain.
+// Probability P^T of K/V row gj against query column col (global position
+// q0g + step*col), log2 domain.
 struct ColCtx {
   float c2, slope2, lin_base, lin_sl;
-  int64_t gj, q0g;
+  int64_t gj, q0g, step;
   bool causal, alibi;
 };
 
@@ -183,7 +188,7 @@ __device__ __forceinline__ float prob(float s, float lse2, int col, int colh, co
   } else if constexpr (kKind == kLinear) {
     return tc::ex2(fmaf(s, c.c2, fmaf(c.lin_sl, (float)colh, c.lin_base) - lse2));
   } else {
-    const int64_t gi = c.q0g + col;
+    const int64_t gi = c.q0g + c.step * col;
     const bool vis = !c.causal || c.gj <= gi;
     float v = s * c.c2 - lse2;
     if (c.alibi) v -= c.slope2 * (float)(gi > c.gj ? gi - c.gj : c.gj - gi);
@@ -245,7 +250,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t bh = L / ntiles;
   const int64_t tile = L - bh * ntiles;
   const int hh = (int)(bh % P.H);
-  const int64_t kp0 = P.causal ? m.inv(tile * kBM) : tile * kBM;
+  // (heaviest first under causal where tiles hold consecutive positions; strided
+  // shards are balanced already)
+  const int64_t kp0 = P.causal && m.layout != RA_LAYOUT_STRIDED ? m.inv(tile * kBM) : tile * kBM;
   const int64_t kg0 = m.g(kp0);
   const int32_t s0 = m.shard(kp0);
 
@@ -414,13 +421,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = warp >> 2;   // Q column half: 64*h ..
     const int krow = qd * 32 + lane;
     const uint32_t t_row = tmem + ((uint32_t)(qd * 32) << 16);
-    const int64_t gj = kg0 + krow;  // K/V tiles are contiguous
+    const int64_t gstep = m.run_step();
+    const int64_t gj = kg0 + gstep * krow;  // K/V tiles are arithmetic runs
     const bool alibi = P.slopes != nullptr;
     const float slope2 = alibi ? P.slopes[hh] * kLog2e : 0.f;
     ColCtx cc;
     cc.c2 = P.c2;
     cc.slope2 = slope2;
     cc.gj = gj;
+    cc.step = gstep;
     cc.causal = P.causal != 0;
     cc.alibi = alibi;
     uint8_t* ds_tile = sgen + kOffDS + h * kBoxBytes;
@@ -434,15 +443,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     while (walk.next(qt)) {
       // Tile kind for this K/V row block against this Q tile.
-      const int64_t qgmin = qt.g0, qgmax = qt.g0 + kBM - 1;
-      const int64_t kgmin = kg0, kgmax = kg0 + kBM - 1;
+      const int64_t qgmin = qt.g0, qgmax = qt.g0 + (kBM - 1) * gstep;
+      const int64_t kgmin = kg0, kgmax = kg0 + (kBM - 1) * gstep;
       const bool below = kgmax <= qgmin;                 // every key at or before every query
       const bool above = !cc.causal && kgmin >= qgmax;   // every key at or after every query
       const bool full = cc.causal ? below : (!alibi || below || above);
       const int kind = full ? (alibi ? kLinear : kPlain) : kGeneral;
       cc.q0g = qt.g0;
       // bias of column col: below: -slope (q0g + col - gj); above: -slope (gj - q0g - col)
-      cc.lin_sl = below ? -slope2 : slope2;
+      cc.lin_sl = (below ? -slope2 : slope2) * (float)gstep;
       cc.lin_base = (below ? -slope2 * (float)(qt.g0 - gj) : -slope2 * (float)(gj - qt.g0)) +
                     cc.lin_sl * (float)(64 * h);  // this warp's first column
 
@@ -583,8 +592,7 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
 }  // namespace
 
 bool bwd_tc_supported(int64_t S, int64_t D, int32_t dtype, const SeqMap& m) {
-  const int64_t chunk = m.layout == RA_LAYOUT_ZIGZAG ? m.h : m.c;
-  return dtype == RA_BF16 && D == kD && S >= kBM && chunk % kBM == 0;
+  return dtype == RA_BF16 && D == kD && S >= kBM && m.run() % kBM == 0;
 }
 
 cudaError_t launch_bwd_tc(const AttnArgs& a, const float* lse, const void* dout, const float* dvec,

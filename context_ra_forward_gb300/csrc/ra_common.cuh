@@ -30,16 +30,20 @@ enum KernelId : int32_t { kKernFwdTc = 1, kKernBwdTc = 2, kKernDebug = 3 };
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // ----------------------------------------------------------------------------
-// Sequence -> shard-major slot maps ([CP] §2.1, [ZZ] §Zig Zag, 2N-chunk form)
+// Sequence -> shard-major slot maps ([CP] §2.1, [ZZ] §Zig Zag)
 //   contiguous: slot p holds global position p.
 //   zigzag:     c = S/N slots per shard, h = c/2 per chunk; slot p of shard
 //               r = p div c, offset u = p mod c, holds global position
 //               r*h + u (first chunk, u < h) or (2N-1-r)*h + (u-h) (second).
+//   strided:    shard r holds tokens r, r+N, r+2N, ... ("GPU 0 gets tokens
+//               [0, 4, 8...], GPU 1 gets [1, 5, 9...]"): slot p holds u*N + r.
+// Within one chunk (zigzag), one shard (strided) or anywhere (contiguous) the
+// global positions of consecutive slots form an arithmetic sequence.
 // ----------------------------------------------------------------------------
 struct SeqMap {
   int64_t S;
   int64_t c;   // slots per shard
-  int64_t h;   // tokens per chunk (zigzag) / c (contiguous)
+  int64_t h;   // tokens per chunk (zigzag) / c (otherwise)
   int32_t N;
   int32_t layout;
 
@@ -54,26 +58,43 @@ struct SeqMap {
   }
   // slot -> global position
   __host__ __device__ __forceinline__ int64_t g(int64_t p) const {
-    if (layout != RA_LAYOUT_ZIGZAG) return p;
-    const int64_t r = p / c, u = p - r * c;
-    return u < h ? r * h + u : (2 * (int64_t)N - 1 - r) * h + (u - h);
+    if (layout == RA_LAYOUT_ZIGZAG) {
+      const int64_t r = p / c, u = p - r * c;
+      return u < h ? r * h + u : (2 * (int64_t)N - 1 - r) * h + (u - h);
+    }
+    if (layout == RA_LAYOUT_STRIDED) {
+      const int64_t r = p / c, u = p - r * c;
+      return u * N + r;
+    }
+    return p;
   }
   // global position -> slot
   __host__ __device__ __forceinline__ int64_t inv(int64_t gp) const {
-    if (layout != RA_LAYOUT_ZIGZAG) return gp;
-    const int64_t k = gp / h, u = gp - k * h;
-    return k < N ? k * c + u : (2 * (int64_t)N - 1 - k) * c + h + u;
+    if (layout == RA_LAYOUT_ZIGZAG) {
+      const int64_t k = gp / h, u = gp - k * h;
+      return k < N ? k * c + u : (2 * (int64_t)N - 1 - k) * c + h + u;
+    }
+    if (layout == RA_LAYOUT_STRIDED) {
+      const int64_t u = gp / N, r = gp - u * N;
+      return r * c + u;
+    }
+    return gp;
   }
   __host__ __device__ __forceinline__ int32_t shard(int64_t p) const { return (int32_t)(p / c); }
+  // Slots per run of arithmetic global positions (a chunk or a shard).
+  __host__ __device__ __forceinline__ int64_t run() const { return layout == RA_LAYOUT_ZIGZAG ? h : c; }
+  // Step of the global positions within a run.
+  __host__ __device__ __forceinline__ int64_t run_step() const { return layout == RA_LAYOUT_STRIDED ? N : 1; }
   // Smallest and largest global position held by the slots [p0, p1) (p0 < p1 <= S).
-  // Walks the chunk segments the range touches; each chunk is increasing.
+  // Walks the runs the range touches; each run is increasing.
   __host__ __device__ void grange(int64_t p0, int64_t p1, int64_t& gmin, int64_t& gmax) const {
-    if (layout != RA_LAYOUT_ZIGZAG) { gmin = p0; gmax = p1 - 1; return; }
+    if (layout == RA_LAYOUT_CONTIGUOUS) { gmin = p0; gmax = p1 - 1; return; }
+    const int64_t L = run();
     gmin = INT64_MAX;
     gmax = -1;
     int64_t a = p0;
     while (a < p1) {
-      const int64_t seg_end = (a / h + 1) * h;   // chunks are h slots long in the buffer
+      const int64_t seg_end = (a / L + 1) * L;
       const int64_t b = seg_end < p1 ? seg_end : p1;
       const int64_t ga = g(a), gb = g(b - 1);
       gmin = ga < gmin ? ga : gmin;
@@ -81,11 +102,14 @@ struct SeqMap {
       a = b;
     }
   }
-  // True when the slots [p0, p1) hold consecutive global positions.
-  __host__ __device__ bool contiguous_range(int64_t p0, int64_t p1) const {
-    if (layout != RA_LAYOUT_ZIGZAG) return true;
-    return (p0 / h) == ((p1 - 1) / h);
+  // Step of the global positions over the slots [p0, p1) when they form one
+  // arithmetic sequence (1 = consecutive positions), 0 when they do not.
+  __host__ __device__ int64_t gstep(int64_t p0, int64_t p1) const {
+    if (layout == RA_LAYOUT_CONTIGUOUS || p1 - p0 <= 1) return 1;
+    return (p0 / run()) == ((p1 - 1) / run()) ? run_step() : 0;
   }
+  // True when the slots [p0, p1) hold consecutive global positions.
+  __host__ __device__ bool contiguous_range(int64_t p0, int64_t p1) const { return gstep(p0, p1) == 1; }
 };
 
 // ----------------------------------------------------------------------------

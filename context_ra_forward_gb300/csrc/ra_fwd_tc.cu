@@ -85,7 +85,7 @@ struct FwdParams {
   int32_t H;
   int32_t BH;
   int32_t causal;
-  int32_t aligned;      // every 256-row query pair and 128-row tile lies in one chunk
+  int32_t aligned;      // every 256-row query pair and 128-row tile lies in one run
   int32_t heavy_first;  // causal + aligned: CTAs ordered by decreasing work
   const float* slopes;
   float c2;             // softmax scale * log2(e)
@@ -96,10 +96,10 @@ struct FwdParams {
 
 struct TileInfo {
   int64_t p0;    // first shard-major slot of the K/V tile
-  int64_t gk0;   // global position of p0 when the tile is contiguous
+  int64_t gk0;   // global position of p0 when the tile's positions are arithmetic
+  int64_t step;  // their step (1 = consecutive; N inside a strided shard); 0 = irregular
   int64_t gmin, gmax;
   int32_t valid; // rows of the tile below S
-  bool contig;   // consecutive global positions
 };
 
 // Walks the K/V tiles of one query pair in ring order, skipping tiles every key
@@ -146,22 +146,24 @@ struct KvWalk {
         } else {
           len = m.c;
           seg_p0 = s * m.c;
-          seg_g0 = seg_p0;
+          seg_g0 = m.g(seg_p0);  // s for strided, s*c for contiguous
         }
+        const int64_t span = kBM * m.run_step();  // global positions one tile covers
         int64_t cnt = len / kBM;
         if (P->causal) {
-          const int64_t vis = qgmax < seg_g0 ? 0 : (qgmax - seg_g0) / kBM + 1;
+          const int64_t vis = qgmax < seg_g0 ? 0 : (qgmax - seg_g0) / span + 1;
           cnt = vis < cnt ? vis : cnt;
         }
         ti = 0;
         tend = cnt;
       }
+      const int64_t step = m.run_step();
       out.p0 = seg_p0 + ti * kBM;
-      out.gk0 = seg_g0 + ti * kBM;
+      out.gk0 = seg_g0 + ti * kBM * step;
+      out.step = step;
       out.gmin = out.gk0;
-      out.gmax = out.gk0 + kBM - 1;
+      out.gmax = out.gk0 + (kBM - 1) * step;
       out.valid = kBM;
-      out.contig = true;
       ++ti;
       return true;
     }
@@ -180,8 +182,8 @@ struct KvWalk {
       m.grange(p0, p1, gmin, gmax);
       if (P->causal && gmin > qgmax) continue;
       out.p0 = p0;
-      out.contig = m.contiguous_range(p0, p1);
-      out.gk0 = out.contig ? m.g(p0) : -1;
+      out.step = m.gstep(p0, p1);
+      out.gk0 = out.step ? m.g(p0) : -1;
       out.gmin = gmin;
       out.gmax = gmax;
       out.valid = (int32_t)(p1 - p0);
@@ -193,9 +195,9 @@ struct KvWalk {
 // Per-row context of one K/V tile for the softmax.
 struct RowCtx {
   float c2, sl, base, slope2;
-  int64_t gi, gk0;
+  int64_t gi, gk0, step;
   int32_t valid;
-  bool contig, causal, row_ok, alibi;
+  bool causal, row_ok, alibi;
   const volatile int32_t* gtab;
 };
 
@@ -212,7 +214,7 @@ __device__ __forceinline__ float tile_score(int u, float raw, float lin, const R
   } else if constexpr (kKind == kLinear) {
     return fmaf(raw, c.c2, lin);
   } else {
-    const int64_t gj = c.contig ? c.gk0 + u : (int64_t)c.gtab[u];
+    const int64_t gj = c.step ? c.gk0 + c.step * u : (int64_t)c.gtab[u];
     const bool vis = c.row_ok && u < c.valid && (!c.causal || gj <= c.gi);
     float v = raw * c.c2;
     if (c.alibi) v -= c.slope2 * (float)(c.gi > gj ? c.gi - gj : gj - c.gi);
@@ -486,10 +488,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Classify the tile for this Q tile.
       const bool below = tile.gmax <= qgmin;              // every key at or before every query
       const bool above = !P.causal && tile.gmin >= qgmax; // every key at or after every query
-      bool full = tile_has_rows && tile.valid == kBM && tile.contig && (P.causal ? below : true);
-      if (alibi && full && !P.causal && !(below || above)) full = false;
-      const int kind = full ? (alibi ? kLinear : kPlain) : kGeneral;
-      if (kind == kGeneral && !tile.contig) {
+      // kPlain: every key visible to every row, no bias; kLinear: the same with an
+      // ALiBi bias linear in the column (tile on one side of every query and its
+      // positions arithmetic); kGeneral: element by element.
+      const bool visible_all = tile_has_rows && tile.valid == kBM && (P.causal ? below : true);
+      const int kind = !visible_all ? kGeneral
+                                    : (!alibi ? kPlain : ((below || above) && tile.step != 0 ? kLinear : kGeneral));
+      if (kind == kGeneral && tile.step == 0) {
         // Keys of this tile come from several chunks: the warp maps the 128 slots
         // (four per lane) into its own table.
         __syncwarp();
@@ -502,13 +507,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       RowCtx rc;
       rc.c2 = c2;
-      rc.sl = below ? slope2 : -slope2;
+      rc.sl = (below ? slope2 : -slope2) * (float)tile.step;
       rc.base = below ? slope2 * (float)(tile.gk0 - gi) : slope2 * (float)(gi - tile.gk0);
       rc.slope2 = slope2;
       rc.gi = gi;
       rc.gk0 = tile.gk0;
       rc.valid = tile.valid;
-      rc.contig = tile.contig;
+      rc.step = tile.step;
       rc.causal = P.causal != 0;
       rc.row_ok = row_ok;
       rc.alibi = alibi;
@@ -598,9 +603,12 @@ cudaError_t launch_fwd_tc(const AttnArgs& a, void* o, float* lse, cudaStream_t s
   p.H = (int32_t)a.H;
   p.BH = (int32_t)BH;
   p.causal = a.causal;
-  const int64_t chunk = a.map.layout == RA_LAYOUT_ZIGZAG ? a.map.h : a.map.c;
-  p.aligned = (chunk % 256) == 0;
-  p.heavy_first = p.aligned && a.causal;
+  // aligned: every 256-row query pair and 128-row tile lies in one run of
+  // arithmetic positions (a zig-zag chunk, or a shard otherwise).
+  p.aligned = (a.map.run() % 256) == 0;
+  // Heaviest pairs first under causal, where pairs hold consecutive positions (in
+  // the strided layout every pair already has about the same work).
+  p.heavy_first = p.aligned && a.causal && a.map.layout != RA_LAYOUT_STRIDED;
   p.slopes = a.slopes;
   p.c2 = a.scale * kLog2e;
   p.o = static_cast<__nv_bfloat16*>(o);

@@ -2,7 +2,8 @@
 //
 // [ZZ] "大模型如何訓練百萬 Token 上下文：上下文并行與 Ring Attention" §Zig Zag Ring
 // Attention (interleaved assignment; "the index logic is slightly more involved")
-// and [CP] "百万Token上下文训练的挑战与突破" §2.1 (contiguous split).
+// and [CP] "百万Token上下文训练的挑战与突破" §2.1 (contiguous split); the token-strided
+// assignment is the one [ZZ] §Zig Zag prints ("GPU 0 gets tokens [0, 4, 8...]").
 //
 // Design: HBM-bound copy.  Every thread moves 16-byte chunks; consecutive threads
 // write consecutive chunks of the output (coalesced stores), reading the matching
@@ -35,16 +36,28 @@ __device__ __forceinline__ void st_stream(int4* p, int4 v) {
 // 32-bit closed forms (the host checks S * chunks_per_row < 2^31).
 struct Map32 {
   uint32_t c, h, N;
-  int32_t zigzag;
+  int32_t layout;
   __device__ __forceinline__ uint32_t g(uint32_t p) const {
-    if (!zigzag) return p;
-    const uint32_t r = p / c, u = p - r * c;
-    return u < h ? r * h + u : (2 * N - 1 - r) * h + (u - h);
+    if (layout == RA_LAYOUT_ZIGZAG) {
+      const uint32_t r = p / c, u = p - r * c;
+      return u < h ? r * h + u : (2 * N - 1 - r) * h + (u - h);
+    }
+    if (layout == RA_LAYOUT_STRIDED) {
+      const uint32_t r = p / c, u = p - r * c;
+      return u * N + r;
+    }
+    return p;
   }
   __device__ __forceinline__ uint32_t inv(uint32_t gp) const {
-    if (!zigzag) return gp;
-    const uint32_t k = gp / h, u = gp - k * h;
-    return k < N ? k * c + u : (2 * N - 1 - k) * c + h + u;
+    if (layout == RA_LAYOUT_ZIGZAG) {
+      const uint32_t k = gp / h, u = gp - k * h;
+      return k < N ? k * c + u : (2 * N - 1 - k) * c + h + u;
+    }
+    if (layout == RA_LAYOUT_STRIDED) {
+      const uint32_t u = gp / N, r = gp - u * N;
+      return r * c + u;
+    }
+    return gp;
   }
 };
 
@@ -85,7 +98,7 @@ cudaError_t launch_permute(const void* x, void* y, int64_t BH, int64_t S, int64_
   m.c = (uint32_t)sm.c;
   m.h = (uint32_t)sm.h;
   m.N = (uint32_t)sm.N;
-  m.zigzag = sm.layout == RA_LAYOUT_ZIGZAG;
+  m.layout = sm.layout;
   const int64_t cpr = row_bytes / 16;
   const int64_t per_head = S * cpr;
   const int64_t per_block = kThreads * kUnroll;

@@ -49,6 +49,10 @@ WORKLOADS = {
     "C3": Workload("C3", 1, 32, 65536, 128, "bf16", True, False, 8, "zigzag", False, 3),
     "C4": Workload("C4", 1, 32, 65536, 128, "bf16", True, True, 8, "zigzag", False, 4),
     "C5": Workload("C5", 1, 16, 262144, 128, "bf16", True, False, 16, "zigzag", True, 5),
+    # the same causal workloads with the token-strided assignment the Zig-Zag
+    # section prints ("GPU 0 gets tokens [0, 4, 8...]")
+    "C3S": Workload("C3S", 1, 32, 65536, 128, "bf16", True, False, 8, "strided", False, 3),
+    "C5S": Workload("C5S", 1, 16, 262144, 128, "bf16", True, False, 16, "strided", True, 5),
 }
 
 

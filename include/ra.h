@@ -24,7 +24,9 @@
  *  - Layouts.  RA_LAYOUT_CONTIGUOUS: shard r holds tokens [r*S/N, (r+1)*S/N)
  *    ([CP] §2.1), needs S % N == 0.  RA_LAYOUT_ZIGZAG: the sequence is cut into 2N
  *    chunks of h = S/(2N) tokens; shard r holds chunk r followed by chunk 2N-1-r
- *    ([ZZ] §Zig Zag, 2N-chunk form), needs S % (2N) == 0.
+ *    ([ZZ] §Zig Zag, 2N-chunk form), needs S % (2N) == 0.  RA_LAYOUT_STRIDED: shard r
+ *    holds tokens r, r+N, r+2N, ... ([ZZ] §Zig Zag as printed: "GPU 0 gets tokens
+ *    [0, 4, 8...], GPU 1 gets [1, 5, 9...]"), needs S % N == 0.
  *  - Pointers named "device" are CUDA device pointers (e.g. from PyTorch) and must
  *    be 16-byte aligned (LSE and the slopes: 4-byte aligned).  The caller owns every
  *    buffer; the library allocates no memory at call time and keeps no per-call
@@ -63,10 +65,11 @@ typedef int32_t ra_dtype;
 typedef int32_t ra_layout;
 #define RA_LAYOUT_CONTIGUOUS 0
 #define RA_LAYOUT_ZIGZAG     1
+#define RA_LAYOUT_STRIDED    2
 
 /*
  * ra_index_map — the sequence -> shard assignment as explicit tables (host only).
- * [CP] §2.1 (contiguous), [ZZ] §Zig Zag (2N-chunk interleave).
+ * [CP] §2.1 (contiguous), [ZZ] §Zig Zag (2N-chunk interleave; token-strided).
  *   perm_host[p] = global token position held at shard-major slot p;
  *   inv_host[g]  = shard-major slot of global position g.
  * Both are caller-owned host arrays of S int64 (either may be NULL to skip it).

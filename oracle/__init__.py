@@ -5,7 +5,7 @@ benchmark's CPU-baseline leg may import this package.  It shares no code with
 the CUDA library and the library never calls it.
 """
 from .attention import (  # noqa: F401
-    CONTIGUOUS, ZIGZAG, LAYOUTS, check_split, shard_members, index_maps,
+    CONTIGUOUS, ZIGZAG, STRIDED, LAYOUTS, check_split, shard_members, index_maps,
     causal_pairs_per_shard, attention_forward, attention_backward,
     backward_dq_rows, backward_dkdv_cols, lse_merge, ring_forward,
     online_softmax_rows,

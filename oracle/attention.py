@@ -14,7 +14,9 @@ What each function follows:
       equal pieces, one per device) and [ZZ] §Zig Zag Ring Attention (interleaved
       assignment so every device holds early and late tokens).  The interleaving
       used is the 2N-chunk form: the sequence is cut into 2N equal chunks and
-      shard r holds chunk r followed by chunk 2N-1-r.
+      shard r holds chunk r followed by chunk 2N-1-r.  The token-strided form the
+      same section prints (GPU 0 gets tokens 0, 4, 8, ..., GPU 1 gets 1, 5, 9, ...)
+      is the third layout: shard r holds tokens r, r+N, r+2N, ...
   attention_forward           [LC] §2.1.2 (scores = q.k / sqrt(head dim), then the
       ALiBi bias -|i-j| * slope added) and [ZZ] §Zig Zag (causal: a token sees
       only earlier tokens; the diagonal is visible).  Plain softmax per query row
@@ -43,7 +45,8 @@ import numpy as np
 
 CONTIGUOUS = "contiguous"
 ZIGZAG = "zigzag"
-LAYOUTS = (CONTIGUOUS, ZIGZAG)
+STRIDED = "strided"
+LAYOUTS = (CONTIGUOUS, ZIGZAG, STRIDED)
 
 # Rows of scores materialised at once: a memory bound only (each row's softmax
 # is still taken over its whole key set in one go).
@@ -75,6 +78,9 @@ def shard_members(S: int, N: int, layout: str) -> list[list[int]]:
         for r in range(N):
             for u in range(c):
                 shards[r].append(r * c + u)
+    elif layout == STRIDED:
+        for g in range(S):  # deal the tokens out to the shards in turn
+            shards[g % N].append(g)
     else:
         h = S // (2 * N)
         chunks = [list(range(k * h, (k + 1) * h)) for k in range(2 * N)]

@@ -51,13 +51,15 @@ def _read_golden(name):
 # Index maps
 # ---------------------------------------------------------------------------
 def pin_index_golden(ora):
-    """Hand-written S=16, N=2 shard membership ([CP] §2.1, [ZZ] §Zig Zag)."""
-    for line in _read_golden("zigzag_S16_N2.txt"):
-        head, toks = line.split(":")
-        layout, r = head.split()
-        want = [int(t) for t in toks.split()]
-        got = ora.shard_members(16, 2, layout)[int(r)]
-        assert got == want, (layout, r, got, want)
+    """Hand-written S=16 shard membership: N=2 contiguous / zig-zag ([CP] §2.1,
+    [ZZ] §Zig Zag) and the page's own token-strided example with N=4."""
+    for name, n in (("zigzag_S16_N2.txt", 2), ("strided_S16_N4.txt", 4)):
+        for line in _read_golden(name):
+            head, toks = line.split(":")
+            layout, r = head.split()
+            want = [int(t) for t in toks.split()]
+            got = ora.shard_members(16, n, layout)[int(r)]
+            assert got == want, (layout, r, got, want)
 
 
 def _closed_form_perm(S, N, layout):
@@ -65,6 +67,9 @@ def _closed_form_perm(S, N, layout):
     r = p div c, u = p mod c; g = r h + u if u < h else (2N-1-r) h + (u - h)."""
     if layout == "contiguous":
         return np.arange(S)
+    if layout == "strided":  # slot p of shard r = p div c, offset u = p mod c: u N + r
+        c = S // N
+        return (np.arange(S) % c) * N + np.arange(S) // c
     c, h = S // N, S // (2 * N)
     p = np.arange(S)
     r, u = p // c, p % c
@@ -76,7 +81,7 @@ def pin_index_bijection(ora):
     loop-built zig-zag map equals the closed form, and every zig-zag shard holds
     early (< S/2) and late (>= S/2) tokens ([ZZ] §Zig Zag)."""
     for S, N in [(2, 1), (8, 1), (16, 2), (24, 3), (64, 4), (1024, 4), (96, 8), (128, 64)]:
-        for layout in ("contiguous", "zigzag"):
+        for layout in ("contiguous", "zigzag", "strided"):
             perm, inv = ora.index_maps(S, N, layout)
             assert sorted(perm.tolist()) == list(range(S))
             assert np.array_equal(inv[perm], np.arange(S))
@@ -87,6 +92,8 @@ def pin_index_bijection(ora):
             else:
                 for shard in ora.shard_members(S, N, layout):
                     assert min(shard) < S // 2 <= max(shard)
+            if layout == "strided":  # consecutive tokens land on consecutive shards
+                assert all(inv[g] // (S // N) == g % N for g in range(S))
 
 
 # ---------------------------------------------------------------------------
@@ -100,7 +107,7 @@ def pin_balance(ora):
         layout, *vals = line.split()
         assert ora.causal_pairs_per_shard(16, 2, layout) == [int(x) for x in vals]
     for S, N in [(16, 2), (64, 4), (96, 3), (256, 8)]:
-        for layout in ("contiguous", "zigzag"):
+        for layout in ("contiguous", "zigzag", "strided"):
             got = ora.causal_pairs_per_shard(S, N, layout)
             members = ora.shard_members(S, N, layout)
             brute = []
@@ -119,6 +126,9 @@ def pin_balance(ora):
         zz = ora.causal_pairs_per_shard(S, N, "zigzag")
         assert contig == [c * c * r + c * (c + 1) // 2 for r in range(N)]
         assert zz == [h * h * (2 * N - 1) + h * (h + 1)] * N
+        # strided: shard r holds u N + r, u < c: sum of (u N + r + 1) = N c(c-1)/2 + c(r+1)
+        assert ora.causal_pairs_per_shard(S, N, "strided") == [N * c * (c - 1) // 2 + c * (r + 1)
+                                                                for r in range(N)]
     assert ora.causal_pairs_per_shard(65536, 8, "contiguous")[0] == 33_558_528
     assert ora.causal_pairs_per_shard(65536, 8, "contiguous")[7] == 503_320_576
     assert ora.causal_pairs_per_shard(65536, 8, "zigzag")[3] == 268_439_552
@@ -298,7 +308,7 @@ def pin_ring_forward(ora):
     B, H, S, D = 1, 2, 48, 8
     q, k, v = _qkv(B, H, S, D, 32)
     sl = _slopes(H)
-    for N, layout, causal in itertools.product([1, 2, 3], ["contiguous", "zigzag"], [False, True]):
+    for N, layout, causal in itertools.product([1, 2, 3], ["contiguous", "zigzag", "strided"], [False, True]):
         o_ref, l_ref = ora.attention_forward(q, k, v, causal=causal, scale=0.3, slopes=sl)
         o, l = ora.ring_forward(q, k, v, causal=causal, scale=0.3, slopes=sl, N=N, layout=layout)
         assert np.max(np.abs(o - o_ref)) < 1e-12 and np.max(np.abs(l - l_ref)) < 1e-12

@@ -40,7 +40,8 @@ def test_status_strings(L):
 
 
 @pytest.mark.parametrize("S,N,layout", [(16, 2, "zigzag"), (1024, 4, "zigzag"), (96, 3, "contiguous"),
-                                        (65536, 8, "zigzag"), (24, 12, "zigzag"), (10, 1, "contiguous")])
+                                        (65536, 8, "zigzag"), (24, 12, "zigzag"), (10, 1, "contiguous"),
+                                        (16, 4, "strided"), (1200, 3, "strided"), (65536, 8, "strided")])
 def test_index_map_matches_oracle_bit_exact(L, S, N, layout):
     from context_ra_forward_gb300 import binding
     perm, inv = binding.index_map(S, N, layout)
@@ -54,6 +55,7 @@ def test_index_map_rejects(L):
     assert L.ra_index_map(10, 3, 0, buf.ctypes.data, None) == -1
     assert L.ra_index_map(8, 0, 0, buf.ctypes.data, None) == -1
     assert L.ra_index_map(8, 2, 7, buf.ctypes.data, None) == -2
+    assert L.ra_index_map(10, 4, 2, buf.ctypes.data, None) == -1   # strided: 10 % 4 != 0
     assert L.ra_index_map(0, 2, 1, None, None) == 0
 
 

@@ -17,6 +17,10 @@ CASES = [
     ("tail", "bf16", True, True, 4, "contiguous", 1, 1, 1000, 128),
     ("d64", "bf16", True, False, 2, "zigzag", 1, 2, 512, 64),
     ("f32", "f32", True, True, 4, "zigzag", 1, 2, 1024, 64),
+    ("strided", "bf16", True, False, 8, "strided", 1, 2, 2048, 128),
+    ("strided_alibi", "bf16", True, True, 4, "strided", 1, 2, 2048, 128),
+    ("strided_nc_alibi", "bf16", False, True, 2, "strided", 1, 1, 1024, 128),
+    ("strided_ragged", "bf16", True, False, 3, "strided", 1, 2, 1200, 128),
 ]
 
 

@@ -48,6 +48,12 @@ RAGGED = [
     ("f32_nc", "f32", False, False, 3, "contiguous", 1, 2, 300, 64),
     ("n_eq_half_s", "bf16", True, False, 64, "zigzag", 1, 1, 256, 128),  # chunk = 2 tokens
     ("batch_heads", "bf16", True, False, 2, "zigzag", 3, 5, 512, 128),
+    # token-strided layout: shard r holds tokens r, r+N, ...
+    ("st_aligned", "bf16", True, False, 4, "strided", 1, 2, 2048, 128),     # 512 slots per shard
+    ("st_alibi", "bf16", True, True, 8, "strided", 1, 2, 4096, 128),
+    ("st_nc_alibi", "bf16", False, True, 2, "strided", 1, 2, 1024, 128),
+    ("st_ragged", "bf16", True, True, 3, "strided", 1, 2, 1200, 128),      # 400 slots: tiles straddle shards
+    ("st_f32", "f32", True, True, 4, "strided", 1, 2, 512, 64),
 ]
 
 
@@ -62,7 +68,7 @@ def test_layout_and_n_independence():
     """O and LSE in original order do not depend on N or the layout (the ring is
     a visit order; the merge is exact up to rounding)."""
     base = None
-    for N, layout in [(1, "contiguous"), (8, "zigzag"), (4, "contiguous"), (16, "zigzag")]:
+    for N, layout in [(1, "contiguous"), (8, "zigzag"), (4, "contiguous"), (16, "zigzag"), (8, "strided")]:
         w = inputs.Workload("x", 1, 2, 4096, 128, "bf16", True, False, N, layout, False, 21)
         out, _, _, _ = run_case(w, backward=False)
         if base is None:

@@ -18,7 +18,8 @@ def _bits(t):
                                      (torch.bfloat16, 64), (torch.bfloat16, 128)])
 @pytest.mark.parametrize("S,N,layout", [(1024, 4, "zigzag"), (1200, 3, "zigzag"), (1000, 4, "contiguous"),
                                         (8, 4, "zigzag"), (2, 1, "zigzag"), (4096, 8, "zigzag"),
-                                        (768, 1, "contiguous")])
+                                        (768, 1, "contiguous"), (16, 4, "strided"), (1200, 3, "strided"),
+                                        (4096, 8, "strided")])
 def test_permute_bit_exact(dtype, D, S, N, layout):
     import context_ra_forward_gb300 as ra
     x = inputs.randn((2, 3, S, D), 77 + S, dtype).cuda()

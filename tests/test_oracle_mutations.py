@@ -35,6 +35,7 @@ MUTATIONS = {
                               "alpha = np.where(np.isfinite(m), np.exp(ref - m), 0.0)"),
     "ring_direction_skips": ("steps = [(r - t) % N for t in range(N)]", "steps = [(r - t) % N for t in range(1, N)]"),
     "pairs_off_by_one": ("int(sum(g + 1 for g in shard))", "int(sum(g for g in shard))"),
+    "strided_blocks": ("shards[g % N].append(g)", "shards[g // (S // N)].append(g)"),
 }
 
 
