@@ -308,6 +308,52 @@ def side_config(cfg, dev, iters=3):
     return {"forward_ms": round(ms, 3), "forward_tflops": round(fwd / ms / 1e9, 1)}
 
 
+def partials_config(cfg, dev, iters=2):
+    """The separate-partials dataflow of a multi-device ring on one GPU: N ring-step
+    launches writing fp32 partials plus N-1 LSE merges, against the same useful
+    flops as the fused forward (context for the single line)."""
+    import context_ra_forward_gb300 as ra
+    from context_ra_forward_gb300 import inputs
+    w = inputs.WORKLOADS[cfg]
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed)
+    shape = (w.B, w.H, w.S, w.D)
+    q, k, v = (torch.randn(shape, generator=g, device=dev).to(torch.bfloat16) for _ in range(3))
+    acc_o = torch.empty(shape, dtype=torch.float32, device=dev)
+    acc_l = torch.empty(shape[:3], dtype=torch.float32, device=dev)
+    st_o = torch.empty_like(acc_o)
+    st_l = torch.empty_like(acc_l)
+    out = torch.empty_like(q)
+
+    def once(merge_events=None):
+        ra.forward_ring_step(q, k, v, 0, causal=w.causal, N=w.N, layout=w.layout, out=acc_o, lse=acc_l)
+        for t in range(1, w.N):
+            ra.forward_ring_step(q, k, v, t, causal=w.causal, N=w.N, layout=w.layout, out=st_o, lse=st_l)
+            if merge_events is not None:
+                merge_events[0].record()
+            ra.lse_merge(acc_o, acc_l, st_o, st_l, out=out if t == w.N - 1 else None)
+            if merge_events is not None:
+                merge_events[1].record()
+
+    once()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        once()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / iters
+    m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    once((m0, m1))
+    torch.cuda.synchronize()
+    merge_ms = m0.elapsed_time(m1)  # the last merge (it also writes the bf16 output)
+    merge_bytes = w.B * w.H * w.S * (w.D * 4 * 3 + w.D * 2 + 4 * 3)
+    fwd, _ = flops_of(w, backward=False)
+    return {"steps": w.N, "total_ms": round(ms, 3), "tflops": round(fwd / ms / 1e9, 1),
+            "merge_ms": round(merge_ms, 3), "merge_gbs": round(merge_bytes / merge_ms / 1e6, 1)}
+
+
 def run_ours(args, w):
     import context_ra_forward_gb300 as ra
     from context_ra_forward_gb300 import inputs
@@ -403,6 +449,7 @@ def run_ours(args, w):
         for c in ("C2", "C3", "C4", "C3S"):
             if c != w.name:
                 side[c] = side_config(c, dev)
+        side["C3_separate_partials"] = partials_config("C3", dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

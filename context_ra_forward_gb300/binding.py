@@ -58,6 +58,11 @@ def lib() -> ctypes.CDLL:
     L.ra_check_device_status.argtypes = [_vp, _vp]
     L.ra_forward_path.argtypes = [_i64, _i64, _i64, _i64, _i32, _i32, _i32]
     L.ra_debug_wait_timeout.argtypes = [_i32, _vp]
+    L.ra_forward_ring_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32, _i32, _vp,
+                                       _f32, _i32, _i32, _i32, _vp]
+    L.ra_forward_ring_step.restype = ctypes.c_int32
+    L.ra_lse_merge.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _i64, _vp]
+    L.ra_lse_merge.restype = ctypes.c_int32
     L.ra_debug_wait_sites.argtypes = [_vp, _i32]
     L.ra_debug_wait_sites.restype = ctypes.c_int32
     L.ra_last_cuda_error.argtypes = []
@@ -229,3 +234,34 @@ def debug_wait_sites():
     buf = (ctypes.c_int32 * n)()
     lib().ra_debug_wait_sites(ctypes.cast(buf, ctypes.c_void_p), n)
     return [None if v == 0 else ((v >> 24) & 0xff, (v >> 16) & 1, v & 0xffff) for v in buf]
+
+
+def forward_ring_step(q, k, v, step, *, causal=False, alibi_slopes=None, softmax_scale=None, N=1,
+                      layout="contiguous", out=None, lse=None, stream=None):
+    """One ring step as a separate partial (ra_forward_ring_step): returns fp32
+    (o_step, lse_step) for the queries of every shard r against the K/V of shard
+    (r - step) mod N."""
+    B, H, S, D = _bhsd(q, "q")
+    for t, n in ((k, "k"), (v, "v")):
+        if _bhsd(t, n) != q.shape or t.dtype != q.dtype:
+            raise ValueError(f"{n} must match q in shape and dtype")
+    o = torch.empty((B, H, S, D), dtype=torch.float32, device=q.device) if out is None else out
+    lse_t = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if lse is None else lse
+    scale = 0.0 if softmax_scale is None else float(softmax_scale)
+    _check(lib().ra_forward_ring_step(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse_t), B, H, S, D,
+                                      DTYPES[q.dtype], int(bool(causal)), _ptr(alibi_slopes), scale, N,
+                                      _layout(layout), int(step), _stream(stream)), "ra_forward_ring_step")
+    return o, lse_t
+
+
+def lse_merge(o_acc, lse_acc, o_step, lse_step, out=None, stream=None):
+    """Merge a ring-step partial into the accumulated one in place (ra_lse_merge);
+    `out` (fp32 or bf16, optional) also receives the merged O."""
+    B, H, S, D = o_acc.shape
+    for t, n in ((o_acc, "o_acc"), (o_step, "o_step")):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() or t.shape != o_acc.shape:
+            raise ValueError(f"{n} must be a contiguous fp32 CUDA tensor [B, H, S, D]")
+    out_dt = DTYPES[out.dtype] if out is not None else 0
+    _check(lib().ra_lse_merge(_ptr(o_acc), _ptr(lse_acc), _ptr(o_step), _ptr(lse_step), _ptr(out), out_dt,
+                              B, H, S, D, _stream(stream)), "ra_lse_merge")
+    return o_acc, lse_acc

@@ -62,6 +62,12 @@ bool overlaps(const void* a, const void* b, size_t bytes) {
   return x < y + bytes && y < x + bytes;
 }
 
+// [a, a + na) and [b, b + nb) intersect
+bool overlaps2(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
 thread_local cudaError_t g_last_cuda_error = cudaSuccess;
 
 ra_status from_cuda(cudaError_t e) {
@@ -110,6 +116,9 @@ ra_status attn_args(const void* q, const void* k, const void* v, int64_t B, int6
   a->scale = resolve_scale(scale, D);
   if (!(a->scale > 0.f) || !isfinite(a->scale)) return RA_ERR_INVALID_ARG;
   a->map = ra::SeqMap::make(S, N, layout);
+  a->t_begin = 0;
+  a->t_end = N;
+  a->o_f32 = nullptr;
   return status_word(&a->status);
 }
 
@@ -197,6 +206,54 @@ ra_status ra_forward(const void* q, const void* k, const void* v, void* o, float
   return from_cuda(ra::launch_fwd_simt(a, o, lse, st));
 }
 
+ra_status ra_forward_ring_step(const void* q, const void* k, const void* v, float* o_step, float* lse_step,
+                               int64_t B, int64_t H, int64_t S, int64_t D, ra_dtype dt, int32_t causal,
+                               const float* slopes, float scale, int32_t N, ra_layout layout, int32_t step,
+                               void* stream) {
+  ra_status s = check_sizes(B, H, S, D, dt, N, layout);
+  if (s != RA_OK) return s;
+  if (!(scale <= 0.f || isfinite(scale))) return RA_ERR_INVALID_ARG;
+  if (step < 0 || step >= N) return RA_ERR_INVALID_ARG;
+  if (B == 0 || H == 0 || S == 0) return RA_OK;
+  const ra::SeqMap m = ra::SeqMap::make(S, N, layout);
+  // every 256-row query block and 128-row key tile must lie inside one shard run
+  if (m.run() % 256 != 0) return RA_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !o_step || !lse_step) return RA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o_step, 16)) return RA_ERR_MISALIGNED;
+  if (!aligned(lse_step, 4) || (slopes && !aligned(slopes, 4))) return RA_ERR_MISALIGNED;
+  const size_t in_bytes = (size_t)(B * H * S * D * elem_bytes(dt));
+  const size_t out_bytes = (size_t)(B * H * S * D * 4);
+  if (overlaps2(o_step, out_bytes, q, in_bytes) || overlaps2(o_step, out_bytes, k, in_bytes) ||
+      overlaps2(o_step, out_bytes, v, in_bytes))
+    return RA_ERR_INVALID_ARG;
+  if (!is_sm103()) return RA_ERR_UNSUPPORTED;
+  ra::AttnArgs a;
+  s = attn_args(q, k, v, B, H, S, D, dt, causal, slopes, scale, N, layout, &a);
+  if (s != RA_OK) return s;
+  a.t_begin = step;
+  a.t_end = step + 1;
+  a.o_f32 = o_step;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (ra::fwd_tc_supported(S, D, dt)) return from_cuda(ra::launch_fwd_tc(a, nullptr, lse_step, st));
+  return from_cuda(ra::launch_fwd_simt(a, nullptr, lse_step, st));
+}
+
+ra_status ra_lse_merge(float* o_acc, float* lse_acc, const float* o_step, const float* lse_step, void* out,
+                       ra_dtype out_dtype, int64_t B, int64_t H, int64_t S, int64_t D, void* stream) {
+  if (B < 0 || H < 0 || S < 0) return RA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return RA_ERR_UNSUPPORTED;
+  if (out && out_dtype != RA_F32 && out_dtype != RA_BF16) return RA_ERR_UNSUPPORTED;
+  if (B == 0 || H == 0 || S == 0) return RA_OK;
+  if (!o_acc || !lse_acc || !o_step || !lse_step) return RA_ERR_INVALID_ARG;
+  if (!aligned(o_acc, 16) || !aligned(o_step, 16) || (out && !aligned(out, 16))) return RA_ERR_MISALIGNED;
+  if (!aligned(lse_acc, 4) || !aligned(lse_step, 4)) return RA_ERR_MISALIGNED;
+  const int64_t rows = B * H * S;
+  if (overlaps(o_acc, o_step, (size_t)(rows * D * 4)) || overlaps(lse_acc, lse_step, (size_t)(rows * 4)))
+    return RA_ERR_INVALID_ARG;
+  return from_cuda(ra::launch_lse_merge(o_acc, lse_acc, o_step, lse_step, out, out_dtype, rows, D,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
 size_t ra_backward_workspace_bytes(int64_t B, int64_t H, int64_t S, int64_t D) {
   if (B <= 0 || H <= 0 || S <= 0 || D <= 0) return 0;
   const size_t rows = (size_t)(B * H * S);
@@ -228,7 +285,7 @@ ra_status ra_backward(const void* q, const void* k, const void* v, const void* o
   for (const void* x : outs) {
     for (const void* y : ins)
       if (overlaps(x, y, bytes)) return RA_ERR_INVALID_ARG;
-    if (overlaps(x, workspace, bytes) || (x != dq && overlaps(x, dq, bytes))) return RA_ERR_INVALID_ARG;
+    if (overlaps2(x, bytes, workspace, ws_bytes) || (x != dq && overlaps(x, dq, bytes))) return RA_ERR_INVALID_ARG;
   }
   if (overlaps(dk, dv, bytes)) return RA_ERR_INVALID_ARG;
   if (!is_sm103()) return RA_ERR_UNSUPPORTED;

@@ -90,8 +90,10 @@ struct FwdParams {
   const float* slopes;
   float c2;             // softmax scale * log2(e)
   __nv_bfloat16* o;
+  float* o_f32;         // when set: O as fp32 (a ring-step partial) instead of o
   float* lse;
   int32_t* status;
+  int32_t t_begin, t_end;  // ring steps visited
 };
 
 struct TileInfo {
@@ -118,7 +120,7 @@ struct KvWalk {
     P = p;
     qgmax = qgmax_;
     r0 = r0_;
-    t = -1;
+    t = p->t_begin - 1;
     seg = 1;  // forces a step to (t = 0, seg = 0)
     ti = tend = 0;
     seg_p0 = seg_g0 = 0;
@@ -131,8 +133,8 @@ struct KvWalk {
       while (ti >= tend) {
         if (++seg >= nseg) {
           seg = 0;
-          if (++t >= m.N) {
-            t = m.N;  // exhausted: every later call returns false too
+          if (++t >= P->t_end) {
+            t = P->t_end;  // exhausted: every later call returns false too
             seg = nseg;
             return false;
           }
@@ -170,7 +172,7 @@ struct KvWalk {
     // General shapes: tiles aligned to the buffer, owned by the shard of their first row.
     while (true) {
       while (ti >= tend) {
-        if (++t >= m.N) return false;
+        if (++t >= P->t_end) return false;
         const int32_t s = (r0 - t + m.N) % m.N;
         ti = (s * m.c + kBM - 1) / kBM;
         tend = ((s + 1) * m.c + kBM - 1) / kBM;
@@ -555,19 +557,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       tc::fence_after_sync();
       const float inv_l = l == 0.f ? 0.f : 1.f / l;  // only l == 0 means "no visible key"; NaN inputs keep l (and O) NaN
-      __nv_bfloat16* orow = P.o + (bh * S + (row_ok ? slot : 0)) * kD;
-#pragma unroll
+      const int64_t orow_off = (bh * S + (row_ok ? slot : 0)) * kD;
+#pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
         tc::tmem_ld32(t_o + 32 * c, r);
         tc::tmem_wait_ld();
+        if (P.o_f32 != nullptr) {  // ring-step partial: fp32 rows
+          if (row_ok) {
+            float4* dst = reinterpret_cast<float4*>(P.o_f32 + orow_off + 32 * c);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              dst[u] = l != 0.f ? make_float4(__uint_as_float(r[4 * u]) * inv_l, __uint_as_float(r[4 * u + 1]) * inv_l,
+                                              __uint_as_float(r[4 * u + 2]) * inv_l, __uint_as_float(r[4 * u + 3]) * inv_l)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          continue;
+        }
         uint32_t pk[16];
 #pragma unroll
         for (int u = 0; u < 16; ++u)
           pk[u] = l != 0.f ? tc::pack_bf16(__uint_as_float(r[2 * u]) * inv_l, __uint_as_float(r[2 * u + 1]) * inv_l)
                           : 0u;
         if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+          uint4* dst = reinterpret_cast<uint4*>(P.o + orow_off + 32 * c);
 #pragma unroll
           for (int u = 0; u < 4; ++u) dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
         }
@@ -612,6 +625,9 @@ cudaError_t launch_fwd_tc(const AttnArgs& a, void* o, float* lse, cudaStream_t s
   p.slopes = a.slopes;
   p.c2 = a.scale * kLog2e;
   p.o = static_cast<__nv_bfloat16*>(o);
+  p.o_f32 = a.o_f32;
+  p.t_begin = a.t_begin;
+  p.t_end = a.t_end;
   p.lse = lse;
   p.status = a.status;
   static std::once_flag once;

@@ -19,6 +19,9 @@ struct AttnArgs {
   float scale;          // resolved softmax scale (> 0)
   SeqMap map;
   int32_t* status;      // device status word
+  int32_t t_begin;      // ring steps [t_begin, t_end) are visited (all: 0, N)
+  int32_t t_end;
+  float* o_f32;         // forward: when set, O goes here as fp32 (a ring-step partial)
 };
 
 // ra_api.cu — counts every kernel launch the library makes (host side).
@@ -45,6 +48,10 @@ bool bwd_tc_supported(int64_t S, int64_t D, int32_t dtype, const SeqMap& m);
 cudaError_t launch_bwd_tc(const AttnArgs& a, const float* lse, const void* dout,
                           const float* dvec, float* dq_acc, void* dq, void* dk, void* dv,
                           cudaStream_t st);
+
+// ra_merge.cu — (o_acc, lse_acc) <- LSE merge with (o_t, lse_t); optional converted copy
+cudaError_t launch_lse_merge(float* o_acc, float* lse_acc, const float* o_t, const float* lse_t, void* out,
+                             int32_t out_dtype, int64_t rows, int64_t D, cudaStream_t st);
 
 // ra_debug.cu
 cudaError_t launch_debug_wait(int32_t limit_us, int32_t* status, cudaStream_t st);

@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(AttnArgs a, T* __res
   m.grange(p_lo, p_hi, qgmin, qgmax);
   const int32_t r0 = m.shard(p_lo);
 
-  for (int32_t t = 0; t < m.N; ++t) {
+  for (int32_t t = a.t_begin; t < a.t_end; ++t) {
     const int32_t s = (r0 - t + m.N) % m.N;  // ring step t meets shard (r0 - t) mod N
     int64_t t0, t1;
     shard_tiles(m, s, t0, t1);
@@ -202,9 +202,12 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(AttnArgs a, T* __res
     T* orow = o + (bh * S + pi) * D;
 #pragma unroll
     for (int t = 0; t < kC; ++t) {
-      store4<T>(orow + 4 * (ql + 4 * t),
-                make_float4(acc[4 * t] * inv_l, acc[4 * t + 1] * inv_l, acc[4 * t + 2] * inv_l,
-                            acc[4 * t + 3] * inv_l));
+      const float4 f = make_float4(acc[4 * t] * inv_l, acc[4 * t + 1] * inv_l, acc[4 * t + 2] * inv_l,
+                                   acc[4 * t + 3] * inv_l);
+      if (a.o_f32 != nullptr)  // ring-step partial: fp32 rows
+        store4<float>(a.o_f32 + (bh * S + pi) * D + 4 * (ql + 4 * t), f);
+      else
+        store4<T>(orow + 4 * (ql + 4 * t), f);
     }
     if (ql == 0) lse[bh * S + pi] = l != 0.f ? (mrun + log2f(l)) * kLn2 : -INFINITY;
   }
@@ -480,6 +483,7 @@ cudaError_t fwd_simt_t(const AttnArgs& a, void* o, float* lse, cudaStream_t st) 
     sub.k = static_cast<const T*>(a.k) + b0 * a.S * D;
     sub.v = static_cast<const T*>(a.v) + b0 * a.S * D;
     dim3 grid((unsigned)((a.S + kRowsPerBlock - 1) / kRowsPerBlock), (unsigned)nb);
+    if (a.o_f32 != nullptr) sub.o_f32 = a.o_f32 + b0 * a.S * D;
     fwd_simt_kernel<T, D><<<grid, kThreads, smem, st>>>(sub, static_cast<T*>(o) + b0 * a.S * D,
                                                         lse + b0 * a.S);
     note_launch();

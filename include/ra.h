@@ -123,6 +123,42 @@ ra_status ra_forward(const void* q, const void* k, const void* v, void* o, float
                      int32_t N, ra_layout layout, void* stream);
 
 /*
+ * ra_forward_ring_step — one ring step of the forward as a separate partial result:
+ * the queries of every shard r against the K/V of shard (r - step) mod N only
+ * ([ZZ] §Zig Zag, one ring step; [CP] §3.1: device i works on the K/V received
+ * from device i-1).  This is the dataflow of a multi-device ring, where each
+ * step's partial is merged as the next K/V block arrives (ra_lse_merge).
+ *   q, k, v: as ra_forward (device, [B,H,S,D] `dtype`, shard-major).
+ *   o_step:  device fp32 [B,H,S,D] (written): the partial output, normalised over
+ *            the step's visible keys; 0 for a row that sees none of them.
+ *   lse_step: device fp32 [B,H,S] (written): the step's log-sum-exp (-inf: none).
+ *   step: 0 <= step < N.  Other arguments as ra_forward.
+ * Needs every shard run (S/N slots, or the S/(2N)-token chunks of RA_LAYOUT_ZIGZAG)
+ * to be a multiple of 256 slots, else RA_ERR_UNSUPPORTED.  Errors as ra_forward.
+ */
+ra_status ra_forward_ring_step(const void* q, const void* k, const void* v, float* o_step, float* lse_step,
+                               int64_t B, int64_t H, int64_t S, int64_t D, ra_dtype dtype, int32_t causal,
+                               const float* alibi_slopes, float softmax_scale, int32_t N, ra_layout layout,
+                               int32_t step, void* stream);
+
+/*
+ * ra_lse_merge — merges a partial result into an accumulated one through their
+ * log-sum-exp ([ZZ] §Zig Zag: the partials of the ring steps combine into exact
+ * attention): per row,
+ *   LSE = log(e^lse_acc + e^lse_step),
+ *   O   = e^(lse_acc - LSE) o_acc + e^(lse_step - LSE) o_step,
+ * written back into (o_acc, lse_acc); a side with LSE = -inf contributes nothing.
+ *   o_acc, o_step: device fp32 [B,H,S,D]; lse_acc, lse_step: device fp32 [B,H,S].
+ *   Start the accumulation from the first step's partial (its buffers).
+ *   out: device [B,H,S,D] of `out_dtype` (RA_F32 or RA_BF16) or NULL; when given,
+ *   also receives the merged O (e.g. on the last step).
+ *   D must be 64 or 128.  Any row order works (the merge is per row).
+ * Errors: RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_MISALIGNED, RA_ERR_CUDA.
+ */
+ra_status ra_lse_merge(float* o_acc, float* lse_acc, const float* o_step, const float* lse_step, void* out,
+                       ra_dtype out_dtype, int64_t B, int64_t H, int64_t S, int64_t D, void* stream);
+
+/*
  * ra_backward_workspace_bytes — device scratch ra_backward needs for these sizes:
  * an fp32 [B,H,S] row term D_i = dO_i . O_i and an fp32 [B,H,S,D] dQ accumulator,
  * each 256-byte aligned.  Returns 0 for an empty problem.
