@@ -308,6 +308,33 @@ def side_config(cfg, dev, iters=3):
     return {"forward_ms": round(ms, 3), "forward_tflops": round(fwd / ms / 1e9, 1)}
 
 
+def fp8_config(cfg, dev, iters=3):
+    """Forward-only TFLOP/s of a workload with e4m3 Q/K/V and per-tensor scales
+    (ra_forward_fp8; context for the single line)."""
+    import context_ra_forward_gb300 as ra
+    from context_ra_forward_gb300 import inputs
+    w = inputs.WORKLOADS[cfg]
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed)
+    shape = (w.B, w.H, w.S, w.D)
+    xs = [torch.randn(shape, generator=g, device=dev) for _ in range(3)]
+    scales = [float(x.abs().max()) / inputs.E4M3_MAX for x in xs]
+    q, k, v = ((x / s).to(torch.float8_e4m3fn) for x, s in zip(xs, scales))
+    del xs
+    sl = inputs.alibi_slopes(w.H).to(dev) if w.alibi else None
+    o, lse = ra.forward_fp8(q, k, v, *scales, causal=w.causal, alibi_slopes=sl, N=w.N, layout=w.layout)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        ra.forward_fp8(q, k, v, *scales, causal=w.causal, alibi_slopes=sl, N=w.N, layout=w.layout, out=o, lse=lse)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / iters
+    fwd, _ = flops_of(w, backward=False)
+    return {"dtype": "e4m3", "forward_ms": round(ms, 3), "forward_tflops": round(fwd / ms / 1e9, 1)}
+
+
 def partials_config(cfg, dev, iters=2):
     """The separate-partials dataflow of a multi-device ring on one GPU: N ring-step
     launches writing fp32 partials plus N-1 LSE merges, against the same useful
@@ -450,6 +477,8 @@ def run_ours(args, w):
             if c != w.name:
                 side[c] = side_config(c, dev)
         side["C3_separate_partials"] = partials_config("C3", dev)
+        side["C2_fp8"] = fp8_config("C2", dev)
+        side["C3_fp8"] = fp8_config("C3", dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -20,7 +20,7 @@ RA_OK = 0
 STATUS_NAMES = {0: "RA_OK", -1: "RA_ERR_INVALID_ARG", -2: "RA_ERR_UNSUPPORTED",
                 -3: "RA_ERR_MISALIGNED", -4: "RA_ERR_CUDA", -5: "RA_ERR_TIMEOUT",
                 -6: "RA_ERR_WORKSPACE"}
-DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float8_e4m3fn: 2}
 LAYOUTS = {"contiguous": 0, "zigzag": 1, "strided": 2}
 
 
@@ -58,6 +58,9 @@ def lib() -> ctypes.CDLL:
     L.ra_check_device_status.argtypes = [_vp, _vp]
     L.ra_forward_path.argtypes = [_i64, _i64, _i64, _i64, _i32, _i32, _i32]
     L.ra_debug_wait_timeout.argtypes = [_i32, _vp]
+    L.ra_forward_fp8.argtypes = [_vp, _vp, _vp, _f32, _f32, _f32, _vp, _vp, _i64, _i64, _i64, _i64, _i32,
+                                 _vp, _f32, _i32, _i32, _vp]
+    L.ra_forward_fp8.restype = ctypes.c_int32
     L.ra_forward_ring_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32, _i32, _vp,
                                        _f32, _i32, _i32, _i32, _vp]
     L.ra_forward_ring_step.restype = ctypes.c_int32
@@ -103,7 +106,7 @@ def _bhsd(t: torch.Tensor, name: str):
     if not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous CUDA tensor")
     if t.dtype not in DTYPES:
-        raise ValueError(f"{name}: dtype {t.dtype} not supported (float32 or bfloat16)")
+        raise ValueError(f"{name}: dtype {t.dtype} not supported (float32, bfloat16, float8_e4m3fn)")
     return t.shape
 
 
@@ -265,3 +268,20 @@ def lse_merge(o_acc, lse_acc, o_step, lse_step, out=None, stream=None):
     _check(lib().ra_lse_merge(_ptr(o_acc), _ptr(lse_acc), _ptr(o_step), _ptr(lse_step), _ptr(out), out_dt,
                               B, H, S, D, _stream(stream)), "ra_lse_merge")
     return o_acc, lse_acc
+
+
+def forward_fp8(q, k, v, q_scale, k_scale, v_scale, *, causal=False, alibi_slopes=None, softmax_scale=None,
+                N=1, layout="contiguous", out=None, lse=None, stream=None):
+    """ra_forward_fp8: e4m3 q/k/v (torch.float8_e4m3fn, shard-major) with per-tensor
+    scales; returns (o bf16, lse fp32)."""
+    B, H, S, D = _bhsd(q, "q")
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        if _bhsd(t, n) != q.shape or t.dtype != torch.float8_e4m3fn:
+            raise ValueError(f"{n} must be float8_e4m3fn and match q in shape")
+    o = torch.empty((B, H, S, D), dtype=torch.bfloat16, device=q.device) if out is None else out
+    lse_t = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if lse is None else lse
+    scale = 0.0 if softmax_scale is None else float(softmax_scale)
+    _check(lib().ra_forward_fp8(_ptr(q), _ptr(k), _ptr(v), float(q_scale), float(k_scale), float(v_scale),
+                                _ptr(o), _ptr(lse_t), B, H, S, D, int(bool(causal)), _ptr(alibi_slopes), scale,
+                                N, _layout(layout), _stream(stream)), "ra_forward_fp8")
+    return o, lse_t

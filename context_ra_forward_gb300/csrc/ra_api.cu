@@ -37,13 +37,13 @@ ra_status status_word(int32_t** out) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-int64_t elem_bytes(ra_dtype dt) { return dt == RA_F32 ? 4 : 2; }
+int64_t elem_bytes(ra_dtype dt) { return dt == RA_F32 ? 4 : (dt == RA_E4M3 ? 1 : 2); }
 
 // Shared scalar checks; returns RA_OK or the first error.
 ra_status check_sizes(int64_t B, int64_t H, int64_t S, int64_t D, ra_dtype dt, int32_t N,
                       ra_layout layout) {
   if (B < 0 || H < 0 || S < 0) return RA_ERR_INVALID_ARG;
-  if (dt != RA_F32 && dt != RA_BF16) return RA_ERR_UNSUPPORTED;
+  if (dt != RA_F32 && dt != RA_BF16 && dt != RA_E4M3) return RA_ERR_UNSUPPORTED;
   if (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_ZIGZAG && layout != RA_LAYOUT_STRIDED)
     return RA_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return RA_ERR_UNSUPPORTED;
@@ -119,6 +119,8 @@ ra_status attn_args(const void* q, const void* k, const void* v, int64_t B, int6
   a->t_begin = 0;
   a->t_end = N;
   a->o_f32 = nullptr;
+  a->qk_scale = 1.f;
+  a->v_scale = 1.f;
   return status_word(&a->status);
 }
 
@@ -181,6 +183,7 @@ int32_t ra_forward_path(int64_t B, int64_t H, int64_t S, int64_t D, ra_dtype dt,
                         ra_layout layout) {
   const ra_status s = check_sizes(B, H, S, D, dt, N, layout);
   if (s != RA_OK) return s;
+  if (dt == RA_E4M3 && (D != 128 || S < 128) && B > 0 && H > 0 && S > 0) return RA_ERR_UNSUPPORTED;
   if (B == 0 || H == 0 || S == 0) return 0;
   return ra::fwd_tc_supported(S, D, dt) ? 1 : 2;
 }
@@ -190,6 +193,7 @@ ra_status ra_forward(const void* q, const void* k, const void* v, void* o, float
                      const float* slopes, float scale, int32_t N, ra_layout layout, void* stream) {
   ra_status s = check_sizes(B, H, S, D, dt, N, layout);
   if (s != RA_OK) return s;
+  if (dt == RA_E4M3) return RA_ERR_UNSUPPORTED;  // 8-bit inputs need scales: ra_forward_fp8
   if (!(scale <= 0.f || isfinite(scale))) return RA_ERR_INVALID_ARG;
   if (B == 0 || H == 0 || S == 0) return RA_OK;
   if (!q || !k || !v || !o || !lse) return RA_ERR_INVALID_ARG;
@@ -206,12 +210,40 @@ ra_status ra_forward(const void* q, const void* k, const void* v, void* o, float
   return from_cuda(ra::launch_fwd_simt(a, o, lse, st));
 }
 
+ra_status ra_forward_fp8(const void* q, const void* k, const void* v, float q_scale, float k_scale,
+                         float v_scale, void* o, float* lse, int64_t B, int64_t H, int64_t S, int64_t D,
+                         int32_t causal, const float* slopes, float scale, int32_t N, ra_layout layout,
+                         void* stream) {
+  ra_status s = check_sizes(B, H, S, D, RA_E4M3, N, layout);
+  if (s != RA_OK) return s;
+  if (!(scale <= 0.f || isfinite(scale))) return RA_ERR_INVALID_ARG;
+  if (!(q_scale > 0.f) || !(k_scale > 0.f) || !(v_scale > 0.f) || !isfinite(q_scale) || !isfinite(k_scale) ||
+      !isfinite(v_scale))
+    return RA_ERR_INVALID_ARG;
+  if (B == 0 || H == 0 || S == 0) return RA_OK;
+  if (!ra::fwd_tc_supported(S, D, RA_E4M3)) return RA_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !o || !lse) return RA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16)) return RA_ERR_MISALIGNED;
+  if (!aligned(lse, 4) || (slopes && !aligned(slopes, 4))) return RA_ERR_MISALIGNED;
+  const size_t in_bytes = (size_t)(B * H * S * D), out_bytes = 2 * in_bytes;
+  if (overlaps2(o, out_bytes, q, in_bytes) || overlaps2(o, out_bytes, k, in_bytes) || overlaps2(o, out_bytes, v, in_bytes))
+    return RA_ERR_INVALID_ARG;
+  if (!is_sm103()) return RA_ERR_UNSUPPORTED;
+  ra::AttnArgs a;
+  s = attn_args(q, k, v, B, H, S, D, RA_E4M3, causal, slopes, scale, N, layout, &a);
+  if (s != RA_OK) return s;
+  a.qk_scale = q_scale * k_scale;
+  a.v_scale = v_scale;
+  return from_cuda(ra::launch_fwd_tc(a, o, lse, static_cast<cudaStream_t>(stream)));
+}
+
 ra_status ra_forward_ring_step(const void* q, const void* k, const void* v, float* o_step, float* lse_step,
                                int64_t B, int64_t H, int64_t S, int64_t D, ra_dtype dt, int32_t causal,
                                const float* slopes, float scale, int32_t N, ra_layout layout, int32_t step,
                                void* stream) {
   ra_status s = check_sizes(B, H, S, D, dt, N, layout);
   if (s != RA_OK) return s;
+  if (dt == RA_E4M3) return RA_ERR_UNSUPPORTED;  // 8-bit inputs need scales: ra_forward_fp8
   if (!(scale <= 0.f || isfinite(scale))) return RA_ERR_INVALID_ARG;
   if (step < 0 || step >= N) return RA_ERR_INVALID_ARG;
   if (B == 0 || H == 0 || S == 0) return RA_OK;
@@ -269,6 +301,7 @@ ra_status ra_backward(const void* q, const void* k, const void* v, const void* o
                       ra_layout layout, void* stream) {
   ra_status s = check_sizes(B, H, S, D, dt, N, layout);
   if (s != RA_OK) return s;
+  if (dt == RA_E4M3) return RA_ERR_UNSUPPORTED;  // 8-bit inputs need scales: ra_forward_fp8
   if (!(scale <= 0.f || isfinite(scale))) return RA_ERR_INVALID_ARG;
   if (B == 0 || H == 0 || S == 0) return RA_OK;
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return RA_ERR_INVALID_ARG;

@@ -110,14 +110,17 @@ struct QTile {
 // Q tiles that see a K/V tile, in ring order; every 128-row tile lies inside one
 // run (a zig-zag chunk, or a shard otherwise, a multiple of 128 slots long), so
 // its global positions are g0, g0 + step, ... (step 1, or N when strided).
+template <bool kStrided>
 struct QWalk {
   const BwdParams* P;
   int64_t kgmin;
   int32_t s0, t, seg;
   int64_t ti, tend, seg_p0, seg_g0;
+  int64_t step;  // global-position step inside a run: N when strided, else 1
 
   __device__ void init(const BwdParams* p, int64_t kgmin_, int32_t s0_) {
     P = p;
+    step = kStrided ? p->map.N : 1;
     kgmin = kgmin_;
     s0 = s0_;
     t = -1;
@@ -148,7 +151,6 @@ struct QWalk {
         seg_p0 = s * m.c;
         seg_g0 = m.g(seg_p0);  // s for strided, s*c for contiguous
       }
-      const int64_t step = m.run_step();
       tend = len / kBM;
       ti = 0;
       if (P->causal) {
@@ -162,7 +164,7 @@ struct QWalk {
       }
     }
     out.p0 = seg_p0 + ti * kBM;
-    out.g0 = seg_g0 + ti * kBM * P->map.run_step();
+    out.g0 = seg_g0 + ti * kBM * step;
     ++ti;
     return true;
   }
@@ -226,6 +228,7 @@ __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+template <bool kStrided>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -252,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hh = (int)(bh % P.H);
   // (heaviest first under causal where tiles hold consecutive positions; strided
   // shards are balanced already)
-  const int64_t kp0 = P.causal && m.layout != RA_LAYOUT_STRIDED ? m.inv(tile * kBM) : tile * kBM;
+  const int64_t kp0 = P.causal && !kStrided ? m.inv(tile * kBM) : tile * kBM;
   const int64_t kg0 = m.g(kp0);
   const int32_t s0 = m.shard(kp0);
 
@@ -289,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Stage s holds Q and dO of Q tile i (s = i & 1) and, once that tile's MMAs
       // are done, its dQ partial: after the softmax warps have staged it, this warp
       // adds it to the accumulator with one bulk reduce, then refills the stage.
-      QWalk walk;
+      QWalk<kStrided> walk;
       walk.init(&P, kg0, s0);
       QTile qt;
       int64_t stage_p0[2] = {0, 0};
@@ -328,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       const uint32_t kb = sbase + kOffK, vb = sbase + kOffV, dsb = sbase + kOffDS;
-      QWalk walk;
+      QWalk<kStrided> walk;
       walk.init(&P, kg0, s0);
       QTile qt;
       bool ok = mbar_wait(bar(kBarKV), 0, P.status, kKernBwdTc, kSiteKFull);
@@ -421,8 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = warp >> 2;   // Q column half: 64*h ..
     const int krow = qd * 32 + lane;
     const uint32_t t_row = tmem + ((uint32_t)(qd * 32) << 16);
-    const int64_t gstep = m.run_step();
-    const int64_t gj = kg0 + gstep * krow;  // K/V tiles are arithmetic runs
+    const int64_t gstep = kStrided ? m.N : 1;  // compile-time 1 unless strided
+    const int64_t gj = kg0 + gstep * krow;     // K/V tiles are arithmetic runs
     const bool alibi = P.slopes != nullptr;
     const float slope2 = alibi ? P.slopes[hh] * kLog2e : 0.f;
     ColCtx cc;
@@ -436,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float* lse_bh = P.lse + bh * S;
     const float* dvec_bh = P.dvec + bh * S;
 
-    QWalk walk;
+    QWalk<kStrided> walk;
     walk.init(&P, kg0, s0);
     QTile qt;
     int i = 0;
@@ -622,13 +625,20 @@ cudaError_t launch_bwd_tc(const AttnArgs& a, const float* lse, const void* dout,
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    attr_err = cudaFuncSetAttribute(bwd_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kSmemBytes);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(bwd_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t tiles = a.S / kBM;
   const int64_t blocks = tiles * BH;
   if (blocks > INT32_MAX) return cudaErrorInvalidValue;
-  bwd_tc_kernel<<<(unsigned)blocks, kThreads, kSmemBytes, st>>>(tq, tk, tv, tdo, tdq, p);
+  if (a.map.layout == RA_LAYOUT_STRIDED)
+    bwd_tc_kernel<true><<<(unsigned)blocks, kThreads, kSmemBytes, st>>>(tq, tk, tv, tdo, tdq, p);
+  else
+    bwd_tc_kernel<false><<<(unsigned)blocks, kThreads, kSmemBytes, st>>>(tq, tk, tv, tdo, tdq, p);
   note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

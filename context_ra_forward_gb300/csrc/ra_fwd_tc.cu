@@ -1,4 +1,5 @@
-// ra_fwd_tc.cu — tcgen05 tensor-core forward for bf16, head dim 128.
+// ra_fwd_tc.cu — tcgen05 tensor-core forward for bf16 (kind::f16) and e4m3
+// (kind::f8f6f4, per-tensor scales), head dim 128.
 //
 // Pages cited:
 //   [ZZ] "大模型如何訓練百萬 Token 上下文：上下文并行與 Ring Attention" §Zig Zag Ring
@@ -47,19 +48,12 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kD = 128;
 constexpr int kStages = 2;
-constexpr int kTileBytes = kBM * kD * 2;  // one 128 x 128 bf16 tile: 32 KB
-constexpr int kBoxBytes = kTileBytes / 2; // one 128 x 64 box: 16 KB
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;
 
-// Shared memory map (offsets from a 1024-byte aligned base).
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + 2 * kTileBytes;
-constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
-constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
 enum Bar {
   kBarQFull = 0,
   kBarKFull = 1,                  // + stage
@@ -72,12 +66,32 @@ enum Bar {
   kBarFinal = kBarODone + 2,
   kNumBars = kBarFinal + 1
 };
-constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
-constexpr uint32_t kOffGtab = kOffTmemSlot + 16;            // 8 warps x 128 int32 key positions
-constexpr uint32_t kSmemBytes = kOffGtab + 8 * kBM * 4 + 1024;  // + alignment slack
 
-constexpr uint32_t kIdescS = tc::idesc_bf16(128, 128, 0, 0);   // Q (K-major) x K (K-major)
-constexpr uint32_t kIdescPV = tc::idesc_bf16(128, 128, 0, 1);  // P (TMEM) x V (MN-major)
+// Element-type dependent layout.  Shared-memory rows are 128 bytes either way
+// (64 bf16 or 128 e4m3 per box row, 128-byte swizzle); one MMA consumes 32 bytes
+// of K per row (16 bf16 or 32 e4m3).
+template <bool kFp8>
+struct FwdCfg {
+  static constexpr int kElem = kFp8 ? 1 : 2;
+  static constexpr int kTileBytes = kBM * kD * kElem;     // 32 KB bf16, 16 KB e4m3
+  static constexpr int kBoxCols = 128 / kElem;            // elements in a 128-byte row
+  static constexpr int kBoxes = kD / kBoxCols;            // boxes per 128-wide head dim
+  static constexpr int kBoxBytes = kTileBytes / kBoxes;   // 16 KB
+  static constexpr int kKStep = 32 / kElem;               // K per MMA
+  static constexpr int kSteps = kD / kKStep;              // MMAs per Q K^T tile
+  static constexpr int kPvSteps = kBM / kKStep;           // MMAs per P V tile
+  // Shared memory map (offsets from a 1024-byte aligned base).
+  static constexpr uint32_t kOffQ = 0;
+  static constexpr uint32_t kOffK = kOffQ + 2 * kTileBytes;
+  static constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
+  static constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
+  static constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
+  static constexpr uint32_t kOffGtab = kOffTmemSlot + 16;             // 8 warps x 128 int32 key positions
+  static constexpr uint32_t kSmemBytes = kOffGtab + 8 * kBM * 4 + 1024;  // + alignment slack
+  // Q (K-major) x K (K-major); P (TMEM) x V (MN-major)
+  static constexpr uint32_t kIdescS = kFp8 ? tc::idesc_e4m3(128, 128, 0, 0) : tc::idesc_bf16(128, 128, 0, 0);
+  static constexpr uint32_t kIdescPV = kFp8 ? tc::idesc_e4m3(128, 128, 0, 1) : tc::idesc_bf16(128, 128, 0, 1);
+};
 
 struct FwdParams {
   SeqMap map;
@@ -88,7 +102,8 @@ struct FwdParams {
   int32_t aligned;      // every 256-row query pair and 128-row tile lies in one run
   int32_t heavy_first;  // causal + aligned: CTAs ordered by decreasing work
   const float* slopes;
-  float c2;             // softmax scale * log2(e)
+  float c2;             // softmax scale * log2(e) (for e4m3: times the Q and K scales)
+  float o_scale;        // V scale (1 for bf16)
   __nv_bfloat16* o;
   float* o_f32;         // when set: O as fp32 (a ring-step partial) instead of o
   float* lse;
@@ -243,74 +258,109 @@ __device__ __forceinline__ float tile_max(uint32_t t_s, const RowCtx& c) {
   return kKind == kPlain ? m * c.c2 : m;
 }
 
-template <int kKind>
+template <int kKind, bool kFp8>
 __device__ __forceinline__ float tile_probs(uint32_t t_s, float mu, const RowCtx& c) {
   float ls[4] = {0.f, 0.f, 0.f, 0.f};
+  auto prob = [&](float s) -> float {
+    if constexpr (kKind == kPlain) return tc::ex2(fmaf(s, c.c2, -mu));
+    else return tc::ex2(s - mu);
+  };
+  if constexpr (!kFp8) {
 #pragma unroll 1
-  for (int hf = 0; hf < 2; ++hf) {
-    uint32_t pk[32];
-    const float lb = fmaf(c.sl, (float)(64 * hf), c.base);
+    for (int hf = 0; hf < 2; ++hf) {
+      uint32_t pk[32];
+      const float lb = fmaf(c.sl, (float)(64 * hf), c.base);
 #pragma unroll
-    for (int ci = 0; ci < 2; ++ci) {
-      uint32_t r[32];
-      tc::tmem_ld32(t_s + 64 * hf + 32 * ci, r);
-      tc::tmem_wait_ld();
+      for (int ci = 0; ci < 2; ++ci) {
+        uint32_t r[32];
+        tc::tmem_ld32(t_s + 64 * hf + 32 * ci, r);
+        tc::tmem_wait_ld();
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int col = 64 * hf + 32 * ci + 2 * u;
-        const float la = fmaf(c.sl, (float)(32 * ci + 2 * u), lb);
-        const float lb1 = fmaf(c.sl, (float)(32 * ci + 2 * u + 1), lb);
-        const float a = tile_score<kKind>(col, __uint_as_float(r[2 * u]), la, c);
-        const float b = tile_score<kKind>(col + 1, __uint_as_float(r[2 * u + 1]), lb1, c);
-        float pa, pb;
-        if constexpr (kKind == kPlain) {
-          pa = tc::ex2(fmaf(a, c.c2, -mu));
-          pb = tc::ex2(fmaf(b, c.c2, -mu));
-        } else {
-          pa = tc::ex2(a - mu);
-          pb = tc::ex2(b - mu);
+        for (int u = 0; u < 16; ++u) {
+          const int col = 64 * hf + 32 * ci + 2 * u;
+          const float la = fmaf(c.sl, (float)(32 * ci + 2 * u), lb);
+          const float lb1 = fmaf(c.sl, (float)(32 * ci + 2 * u + 1), lb);
+          const float pa = prob(tile_score<kKind>(col, __uint_as_float(r[2 * u]), la, c));
+          const float pb = prob(tile_score<kKind>(col + 1, __uint_as_float(r[2 * u + 1]), lb1, c));
+          ls[u & 3] += pa + pb;
+          pk[16 * ci + u] = tc::pack_bf16(pa, pb);
         }
-        ls[u & 3] += pa + pb;
-        pk[16 * ci + u] = tc::pack_bf16(pa, pb);
       }
+      tc::tmem_st32(t_s + 32 * hf, pk);
     }
-    tc::tmem_st32(t_s + 32 * hf, pk);
+  } else {
+    // e4m3: four probabilities per TMEM column; columns 64hf.. of S become P
+    // columns 16hf.. (all inside the S columns read in the first half).
+#pragma unroll 1
+    for (int hf = 0; hf < 2; ++hf) {
+      uint32_t pk[16];
+      const float lb = fmaf(c.sl, (float)(64 * hf), c.base);
+#pragma unroll
+      for (int ci = 0; ci < 2; ++ci) {
+        uint32_t r[32];
+        tc::tmem_ld32(t_s + 64 * hf + 32 * ci, r);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          float pv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int cc = 32 * ci + 4 * u + e;
+            pv[e] = prob(tile_score<kKind>(64 * hf + cc, __uint_as_float(r[4 * u + e]), fmaf(c.sl, (float)cc, lb), c));
+          }
+          ls[u & 3] += (pv[0] + pv[1]) + (pv[2] + pv[3]);
+          pk[8 * ci + u] = tc::pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
+        }
+      }
+      tc::tmem_st16(t_s + 16 * hf, pk);
+    }
   }
   return (ls[0] + ls[1]) + (ls[2] + ls[3]);
 }
 
+template <bool kFp8>
 __device__ __forceinline__ void issue_s(uint32_t tmem, uint32_t sbase, int X, int ks) {
-  const uint32_t qa = sbase + kOffQ + X * kTileBytes;
-  const uint32_t kb = sbase + kOffK + ks * kTileBytes;
+  using C = FwdCfg<kFp8>;
+  const uint32_t qa = sbase + C::kOffQ + X * C::kTileBytes;
+  const uint32_t kb = sbase + C::kOffK + ks * C::kTileBytes;
 #pragma unroll
-  for (int kk = 0; kk < kD / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+  for (int kk = 0; kk < C::kSteps; ++kk) {
+    // four 32-byte K steps per 128-byte swizzle row, then the next box
+    const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
     const uint64_t a = tc::smem_desc(qa + off, 16, 1024);
     const uint64_t b = tc::smem_desc(kb + off, 16, 1024);
-    tc::mma_ss(tmem + X * 128, a, b, kIdescS, kk > 0 ? 1u : 0u);
+    if constexpr (kFp8) tc::mma_ss_f8(tmem + X * 128, a, b, C::kIdescS, kk > 0 ? 1u : 0u);
+    else tc::mma_ss(tmem + X * 128, a, b, C::kIdescS, kk > 0 ? 1u : 0u);
   }
 }
 
+template <bool kFp8>
 __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t sbase, int X, int vs, bool acc) {
-  const uint32_t vb = sbase + kOffV + vs * kTileBytes;
+  using C = FwdCfg<kFp8>;
+  const uint32_t vb = sbase + C::kOffV + vs * C::kTileBytes;
 #pragma unroll
-  for (int kk = 0; kk < kBM / 16; ++kk) {
-    // V is [kv rows, d] with d contiguous: MN-major B.  16 kv rows per step
-    // (2048 bytes), the two 64-wide d halves are one box (16 KB) apart.
-    const uint64_t b = tc::smem_desc(vb + kk * 2048, kBoxBytes, 1024);
-    tc::mma_ts(tmem + 256 + X * 128, tmem + X * 128 + kk * 8, b, kIdescPV, (acc || kk > 0) ? 1u : 0u);
+  for (int kk = 0; kk < C::kPvSteps; ++kk) {
+    // V is [kv rows, d] with d contiguous: MN-major B.  kKStep kv rows per step
+    // (128 bytes each); the 64-wide d halves of bf16 are one box (16 KB) apart.
+    const uint64_t b = tc::smem_desc(vb + kk * C::kKStep * 128, C::kBoxBytes, 1024);
+    if constexpr (kFp8)
+      tc::mma_ts_f8(tmem + 256 + X * 128, tmem + X * 128 + kk * 8, b, C::kIdescPV, (acc || kk > 0) ? 1u : 0u);
+    else
+      tc::mma_ts(tmem + 256 + X * 128, tmem + X * 128 + kk * 8, b, C::kIdescPV, (acc || kk > 0) ? 1u : 0u);
   }
 }
 
+template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ FwdParams P) {
+  using C = FwdCfg<kFp8>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* sgen = smem_raw + (sbase - raw);
-  auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * (uint32_t)i; };
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sgen + kOffTmemSlot);
+  auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * (uint32_t)i; };
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sgen + C::kOffTmemSlot);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const SeqMap& m = P.map;
@@ -341,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == kMmaWarp) {
-    tc::tmem_alloc(sbase + kOffTmemSlot, kTmemCols);
+    tc::tmem_alloc(sbase + C::kOffTmemSlot, kTmemCols);
     tc::tmem_relinquish();
   }
   tc::fence_before_sync();
@@ -355,10 +405,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tma_prefetch_desc(&tm_k);
       tc::tma_prefetch_desc(&tm_v);
       const int32_t z = (int32_t)bh;
-      mbar_arrive_expect_tx(bar(kBarQFull), 2 * kTileBytes);
+      mbar_arrive_expect_tx(bar(kBarQFull), 2 * C::kTileBytes);
       for (int X = 0; X < 2; ++X)
-        for (int hf = 0; hf < 2; ++hf)
-          tc::tma_load_3d(sbase + kOffQ + X * kTileBytes + hf * kBoxBytes, &tm_q, hf * 64,
+        for (int hf = 0; hf < C::kBoxes; ++hf)
+          tc::tma_load_3d(sbase + C::kOffQ + X * C::kTileBytes + hf * C::kBoxBytes, &tm_q, hf * C::kBoxCols,
                           (int32_t)(P0 + X * kBM), z, bar(kBarQFull));
       KvWalk walk;
       walk.init(&P, pair_gmax, r0);
@@ -371,9 +421,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t par = ((j / kStages) & 1) ^ 1;
         ok = mbar_wait(bar(kBarKEmpty + st), par, P.status, kKernFwdTc, kSiteKEmpty);
         if (!ok) break;
-        mbar_arrive_expect_tx(bar(kBarKFull + st), kTileBytes);
-        for (int hf = 0; hf < 2; ++hf)
-          tc::tma_load_3d(sbase + kOffK + st * kTileBytes + hf * kBoxBytes, &tm_k, hf * 64,
+        mbar_arrive_expect_tx(bar(kBarKFull + st), C::kTileBytes);
+        for (int hf = 0; hf < C::kBoxes; ++hf)
+          tc::tma_load_3d(sbase + C::kOffK + st * C::kTileBytes + hf * C::kBoxBytes, &tm_k, hf * C::kBoxCols,
                           (int32_t)tile.p0, z, bar(kBarKFull + st));
         ok = mbar_wait(bar(kBarVEmpty + st), par, P.status, kKernFwdTc, kSiteVEmpty);
         if (!ok) {
@@ -381,9 +431,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           last_v = false;
           break;
         }
-        mbar_arrive_expect_tx(bar(kBarVFull + st), kTileBytes);
-        for (int hf = 0; hf < 2; ++hf)
-          tc::tma_load_3d(sbase + kOffV + st * kTileBytes + hf * kBoxBytes, &tm_v, hf * 64,
+        mbar_arrive_expect_tx(bar(kBarVFull + st), C::kTileBytes);
+        for (int hf = 0; hf < C::kBoxes; ++hf)
+          tc::tma_load_3d(sbase + C::kOffV + st * C::kTileBytes + hf * C::kBoxBytes, &tm_v, hf * C::kBoxCols,
                           (int32_t)tile.p0, z, bar(kBarVFull + st));
         ++j;
       }
@@ -407,9 +457,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(bar(kBarKFull + 0), 0, P.status, kKernFwdTc, kSiteKFull);
         if (ok) {
           tc::fence_after_sync();
-          issue_s(tmem, sbase, 0, 0);
+          issue_s<kFp8>(tmem, sbase, 0, 0);
           tc::mma_commit(bar(kBarSFull + 0));
-          issue_s(tmem, sbase, 1, 0);
+          issue_s<kFp8>(tmem, sbase, 1, 0);
           tc::mma_commit(bar(kBarSFull + 1));
           tc::mma_commit(bar(kBarKEmpty + 0));
         }
@@ -422,12 +472,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                mbar_wait(bar(kBarPFull + 0), j & 1, P.status, kKernFwdTc, kSitePFull);
           if (!ok) break;
           tc::fence_after_sync();
-          issue_pv(tmem, sbase, 0, vs, j > 0);
+          issue_pv<kFp8>(tmem, sbase, 0, vs, j > 0);
           if (more) {
             ok = mbar_wait(bar(kBarKFull + ks), ((j + 1) / kStages) & 1, P.status, kKernFwdTc, kSiteKFull);
             if (!ok) break;
             tc::fence_after_sync();
-            issue_s(tmem, sbase, 0, ks);
+            issue_s<kFp8>(tmem, sbase, 0, ks);
             tc::mma_commit(bar(kBarSFull + 0));
           } else {
             tc::mma_commit(bar(kBarODone + 0));
@@ -435,10 +485,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait(bar(kBarPFull + 1), j & 1, P.status, kKernFwdTc, kSitePFull);
           if (!ok) break;
           tc::fence_after_sync();
-          issue_pv(tmem, sbase, 1, vs, j > 0);
+          issue_pv<kFp8>(tmem, sbase, 1, vs, j > 0);
           tc::mma_commit(bar(kBarVEmpty + vs));
           if (more) {
-            issue_s(tmem, sbase, 1, ks);
+            issue_s<kFp8>(tmem, sbase, 1, ks);
             tc::mma_commit(bar(kBarSFull + 1));
             tc::mma_commit(bar(kBarKEmpty + ks));
           } else {
@@ -475,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float c2 = P.c2;
     const bool alibi = P.slopes != nullptr;
     const float slope2 = alibi ? P.slopes[hh] * kLog2e : 0.f;
-    volatile int32_t* gtab = reinterpret_cast<volatile int32_t*>(sgen + kOffGtab) + warp * kBM;
+    volatile int32_t* gtab = reinterpret_cast<volatile int32_t*>(sgen + C::kOffGtab) + warp * kBM;
 
     float m_ref = -INFINITY, l = 0.f;
     KvWalk walk;
@@ -545,8 +595,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float mu = m_ref == -INFINITY ? 0.f : m_ref;
       // Pass 2: probabilities, packed to bf16 pairs and stored over S columns that
       // have already been read (P column k holds scores 2k, 2k+1).
-      l += kind == kPlain ? tile_probs<kPlain>(t_s, mu, rc)
-                          : (kind == kLinear ? tile_probs<kLinear>(t_s, mu, rc) : tile_probs<kGeneral>(t_s, mu, rc));
+      l += kind == kPlain ? tile_probs<kPlain, kFp8>(t_s, mu, rc)
+                          : (kind == kLinear ? tile_probs<kLinear, kFp8>(t_s, mu, rc) : tile_probs<kGeneral, kFp8>(t_s, mu, rc));
       tc::tmem_wait_st();
       tc::fence_before_sync();
       mbar_arrive(bar(kBarPFull + X));
@@ -556,7 +606,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarODone + X), 0, P.status, kKernFwdTc, kSiteODone));
     if (ok) {
       tc::fence_after_sync();
-      const float inv_l = l == 0.f ? 0.f : 1.f / l;  // only l == 0 means "no visible key"; NaN inputs keep l (and O) NaN
+      // only l == 0 means "no visible key"; NaN inputs keep l (and O) NaN
+      const float inv_l = l == 0.f ? 0.f : P.o_scale / l;
       const int64_t orow_off = (bh * S + (row_ok ? slot : 0)) * kD;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
@@ -600,16 +651,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 bool fwd_tc_supported(int64_t S, int64_t D, int32_t dtype) {
-  return dtype == RA_BF16 && D == kD && S >= kBM;
+  return (dtype == RA_BF16 || dtype == RA_E4M3) && D == kD && S >= kBM;
 }
 
-cudaError_t launch_fwd_tc(const AttnArgs& a, void* o, float* lse, cudaStream_t st) {
+namespace {
+
+template <bool kFp8>
+cudaError_t launch_fwd_tc_t(const AttnArgs& a, void* o, float* lse, cudaStream_t st) {
+  using C = FwdCfg<kFp8>;
   const int64_t BH = a.B * a.H;
   if (BH > INT32_MAX) return cudaErrorInvalidValue;
   CUtensorMap tq, tk, tv;
-  if (!tc::make_tmap_bhsd(&tq, a.q, BH, a.S, a.D, kBM) || !tc::make_tmap_bhsd(&tk, a.k, BH, a.S, a.D, kBM) ||
-      !tc::make_tmap_bhsd(&tv, a.v, BH, a.S, a.D, kBM))
-    return cudaErrorInvalidValue;
+  auto make = [&](CUtensorMap* m, const void* base) {
+    return kFp8 ? tc::make_tmap_bhsd_u8(m, base, BH, a.S, a.D, kBM) : tc::make_tmap_bhsd(m, base, BH, a.S, a.D, kBM);
+  };
+  if (!make(&tq, a.q) || !make(&tk, a.k) || !make(&tv, a.v)) return cudaErrorInvalidValue;
   FwdParams p;
   p.map = a.map;
   p.S = a.S;
@@ -623,7 +679,8 @@ cudaError_t launch_fwd_tc(const AttnArgs& a, void* o, float* lse, cudaStream_t s
   // the strided layout every pair already has about the same work).
   p.heavy_first = p.aligned && a.causal && a.map.layout != RA_LAYOUT_STRIDED;
   p.slopes = a.slopes;
-  p.c2 = a.scale * kLog2e;
+  p.c2 = a.scale * a.qk_scale * kLog2e;
+  p.o_scale = a.v_scale;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.o_f32 = a.o_f32;
   p.t_begin = a.t_begin;
@@ -633,15 +690,22 @@ cudaError_t launch_fwd_tc(const AttnArgs& a, void* o, float* lse, cudaStream_t s
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    attr_err = cudaFuncSetAttribute(fwd_tc_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)C::kSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t pairs = (a.S + 255) / 256;
   const int64_t blocks = pairs * BH;
   if (blocks > INT32_MAX) return cudaErrorInvalidValue;
-  fwd_tc_kernel<<<(unsigned)blocks, kThreads, kSmemBytes, st>>>(tq, tk, tv, p);
+  fwd_tc_kernel<kFp8><<<(unsigned)blocks, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, p);
   note_launch();
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_tc(const AttnArgs& a, void* o, float* lse, cudaStream_t st) {
+  return a.dtype == RA_E4M3 ? launch_fwd_tc_t<true>(a, o, lse, st) : launch_fwd_tc_t<false>(a, o, lse, st);
 }
 
 }  // namespace ra

@@ -22,6 +22,8 @@ struct AttnArgs {
   int32_t t_begin;      // ring steps [t_begin, t_end) are visited (all: 0, N)
   int32_t t_end;
   float* o_f32;         // forward: when set, O goes here as fp32 (a ring-step partial)
+  float qk_scale;       // e4m3 forward: product of the Q and K scales (1 otherwise)
+  float v_scale;        // e4m3 forward: V scale (1 otherwise)
 };
 
 // ra_api.cu — counts every kernel launch the library makes (host side).
@@ -39,7 +41,7 @@ cudaError_t launch_bwd_rowdot(const AttnArgs& a, const void* o, const void* dout
 cudaError_t launch_bwd_simt(const AttnArgs& a, const float* lse, const void* dout,
                             const float* dvec, void* dq, void* dk, void* dv, cudaStream_t st);
 
-// ra_fwd_tc.cu — tcgen05 tensor-core forward (bf16, D = 128)
+// ra_fwd_tc.cu — tcgen05 tensor-core forward (bf16 or e4m3, D = 128)
 bool fwd_tc_supported(int64_t S, int64_t D, int32_t dtype);
 cudaError_t launch_fwd_tc(const AttnArgs& a, void* o, float* lse, cudaStream_t st);
 

@@ -106,6 +106,7 @@ cudaError_t launch_permute(const void* x, void* y, int64_t BH, int64_t S, int64_
   const int4* xi = static_cast<const int4*>(x);
   int4* yi = static_cast<int4*>(y);
   switch (cpr) {
+    case 4:  permute_rows_kernel<2><<<grid, kThreads, 0, st>>>(xi, yi, (uint32_t)S, m, inverse, BH); note_launch(); break;
     case 8:  permute_rows_kernel<3><<<grid, kThreads, 0, st>>>(xi, yi, (uint32_t)S, m, inverse, BH); note_launch(); break;
     case 16: permute_rows_kernel<4><<<grid, kThreads, 0, st>>>(xi, yi, (uint32_t)S, m, inverse, BH); note_launch(); break;
     case 32: permute_rows_kernel<5><<<grid, kThreads, 0, st>>>(xi, yi, (uint32_t)S, m, inverse, BH); note_launch(); break;

@@ -43,6 +43,18 @@ bool make_tmap_bhsd(CUtensorMap* map, const void* base, int64_t BH, int64_t S, i
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_tmap_bhsd_u8(CUtensorMap* map, const void* base, int64_t BH, int64_t S, int64_t D, int box_rows) {
+  EncodeTiledFn fn = encoder();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)D, (cuuint64_t)(S * D)};
+  const cuuint32_t box[3] = {(cuuint32_t)D, (cuuint32_t)box_rows, 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_tmap_bhsd_f32(CUtensorMap* map, const void* base, int64_t BH, int64_t S, int64_t D, int box_rows) {
   EncodeTiledFn fn = encoder();
   if (!fn) return false;

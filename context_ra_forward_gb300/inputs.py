@@ -94,3 +94,21 @@ def alibi_slopes(H: int) -> torch.Tensor:
 def to_f64_numpy(t: torch.Tensor):
     """Exact upcast of a CPU tensor (fp32 or bf16) to a float64 numpy array."""
     return t.detach().to("cpu").to(torch.float64).numpy()
+
+
+E4M3_MAX = 448.0  # largest finite e4m3 value
+
+
+def quantize_e4m3(x: torch.Tensor):
+    """Per-tensor e4m3 quantisation of a CPU tensor: scale = max|x| / 448, returns
+    (x8 as torch.float8_e4m3fn, scale as a Python float).  The value an element
+    stands for is float(x8) * scale."""
+    amax = float(x.float().abs().max())
+    scale = amax / E4M3_MAX if amax > 0 else 1.0
+    x8 = (x.float() / scale).to(torch.float8_e4m3fn)
+    return x8, scale
+
+
+def dequantize_f64(x8: torch.Tensor, scale: float):
+    """Exact value of an e4m3 tensor times its scale, as float64 numpy."""
+    return x8.to(torch.float64).numpy() * scale

@@ -16,7 +16,8 @@
  * --------------------------------
  *  - Tensors are [B, H, S, D] (batch, heads, sequence, head dim), contiguous, D
  *    innermost.  Q/K/V/O/dO/dQ/dK/dV of one call share one dtype: RA_F32 (fp32) or
- *    RA_BF16 (bf16).  LSE is always fp32 [B, H, S].  D must be 64 or 128.
+ *    RA_BF16 (bf16) (ra_forward_fp8 and the permutes also take RA_E4M3).  LSE is
+ *    always fp32 [B, H, S].  D must be 64 or 128.
  *  - Sequence order.  Attention calls take and return tensors in SHARD-MAJOR order:
  *    the N shards' token sequences concatenated, shard 0 first, which is what
  *    ra_zigzag_permute produces.  Global token positions (for the causal mask and
@@ -61,6 +62,7 @@ typedef int32_t ra_status;
 typedef int32_t ra_dtype;
 #define RA_F32   0
 #define RA_BF16  1
+#define RA_E4M3  2   /* 8-bit float (4 exponent, 3 mantissa bits): ra_forward_fp8 and the permutes */
 
 typedef int32_t ra_layout;
 #define RA_LAYOUT_CONTIGUOUS 0
@@ -121,6 +123,25 @@ ra_status ra_forward(const void* q, const void* k, const void* v, void* o, float
                      int64_t B, int64_t H, int64_t S, int64_t D, ra_dtype dtype,
                      int32_t causal, const float* alibi_slopes, float softmax_scale,
                      int32_t N, ra_layout layout, void* stream);
+
+/*
+ * ra_forward_fp8 — ra_forward with e4m3 (8-bit float) Q, K, V and per-tensor
+ * scales: the value of an element is its e4m3 number times the tensor's scale.
+ * Same method and ring order as ra_forward ([ZZ] §Zig Zag, [LC] §3.1.2, §2.1.2);
+ * the products run on the tensor cores at the 8-bit rate (kind::f8f6f4, fp32
+ * accumulation) and the probabilities are rounded to e4m3 for the PV product
+ * (relative rounding error <= 2^-4 per probability), so O carries a relative RMS
+ * error of a few percent; LSE comes from fp32 sums.
+ *   q, k, v: device, [B,H,S,D] e4m3 bytes (RA_E4M3), shard-major.
+ *   q_scale, k_scale, v_scale: > 0, finite.
+ *   o: device bf16 [B,H,S,D] (written); lse: device fp32 [B,H,S] (written).
+ *   D must be 128 and S >= 128 (else RA_ERR_UNSUPPORTED).  Other arguments and
+ *   errors as ra_forward.
+ */
+ra_status ra_forward_fp8(const void* q, const void* k, const void* v, float q_scale, float k_scale,
+                         float v_scale, void* o, float* lse, int64_t B, int64_t H, int64_t S, int64_t D,
+                         int32_t causal, const float* alibi_slopes, float softmax_scale, int32_t N,
+                         ra_layout layout, void* stream);
 
 /*
  * ra_forward_ring_step — one ring step of the forward as a separate partial result:

@@ -1,0 +1,91 @@
+"""ra_forward_fp8 (e4m3 Q/K/V with per-tensor scales) against the fp64 oracle
+evaluated on the exact values the e4m3 inputs stand for.
+
+Tolerance, from the arithmetic: the kernel's products are exact in fp32 and
+LSE comes from fp32 sums, so LSE keeps the bf16 bound (max abs 2e-2).  O also
+carries the rounding of each probability to e4m3 before the PV product: each
+P_j becomes P_j (1 + d_j) with |d_j| <= 2^-4 (three mantissa bits), so
+|dO| = |sum_j P_j d_j v_j| / sum_j P_j <= 2^-4 max|v| per element — reached when
+one key dominates a row (ALiBi) — plus the bf16 rounding of the output (2e-2).
+When many keys share a row the errors average out, which the relative RMS bound
+of 6e-2 (about 1.7 x the 2^-4/sqrt(3) RMS of one rounding) checks."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from context_ra_forward_gb300 import inputs
+from gpu_util import compare, to_orig
+
+pytestmark = pytest.mark.gpu
+
+FP8_REL_RMS = 6e-2
+
+CASES = [
+    # (name, causal, alibi, N, layout, B, H, S)
+    ("zz_causal", True, False, 4, "zigzag", 1, 2, 2048),
+    ("ct_noncausal", False, False, 2, "contiguous", 1, 2, 1024),
+    ("st_alibi", True, True, 4, "strided", 1, 2, 2048),
+    ("zz_ragged", True, True, 3, "zigzag", 1, 2, 1200),
+]
+
+
+def _check(got, ref, max_abs_tol, what):
+    err = got - ref
+    max_abs = float(np.max(np.abs(err)))
+    rel = float(np.linalg.norm(err) / np.linalg.norm(ref))
+    print(f"{what}: max abs {max_abs:.3e} (bound {max_abs_tol:.3e}), rel rms {rel:.3e}")
+    assert max_abs <= max_abs_tol, f"{what}: max abs {max_abs:.3e} > {max_abs_tol:.3e}"
+    assert rel <= FP8_REL_RMS, f"{what}: rel rms {rel:.3e}"
+    return max_abs, rel
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_fp8_forward(case):
+    import context_ra_forward_gb300 as ra
+    name, causal, alibi, N, layout, B, H, S = case
+    D = 128
+    w = inputs.Workload(name, B, H, S, D, "f32", causal, alibi, N, layout, False, 31)
+    x = inputs.make_inputs(w)
+    q8 = {n: inputs.quantize_e4m3(x[n]) for n in ("q", "k", "v")}
+    dev = torch.device("cuda:0")
+    dq = {n: ra.zigzag_permute(q8[n][0].to(dev), N, layout) for n in q8}
+    sl = inputs.alibi_slopes(H).to(dev) if alibi else None
+    o, lse = ra.forward_fp8(dq["q"], dq["k"], dq["v"], q8["q"][1], q8["k"][1], q8["v"][1], causal=causal,
+                            alibi_slopes=sl, N=N, layout=layout)
+    st, detail = ra.check_device_status()
+    assert st == 0, detail
+    f = {n: inputs.dequantize_f64(*q8[n]) for n in q8}
+    o_ref, l_ref = oracle.attention_forward(f["q"], f["k"], f["v"], causal=causal, scale=1.0 / math.sqrt(D),
+                                            slopes=inputs.alibi_slopes(H).double().numpy() if alibi else None)
+    perm, _ = oracle.index_maps(S, N, layout)
+    vmax = float(np.max(np.abs(f["v"])))
+    _check(to_orig(o, perm), o_ref, 2.0 ** -4 * vmax + 2e-2, "O")
+    compare(to_orig(lse, perm), l_ref, "bf16", "LSE")
+
+
+def test_fp8_permute_bit_exact():
+    import context_ra_forward_gb300 as ra
+    x8, _ = inputs.quantize_e4m3(inputs.randn((1, 3, 1024, 128), 5, torch.float32))
+    x = x8.cuda()
+    perm, _ = oracle.index_maps(1024, 4, "zigzag")
+    y = ra.zigzag_permute(x, 4, "zigzag")
+    assert torch.equal(y.view(torch.uint8), x[:, :, torch.as_tensor(perm, device=x.device)].view(torch.uint8))
+    assert torch.equal(ra.unpermute(y, 4, "zigzag").view(torch.uint8), x.view(torch.uint8))
+
+
+def test_fp8_rejects():
+    import context_ra_forward_gb300 as ra
+    q = torch.zeros((1, 1, 256, 64), dtype=torch.float8_e4m3fn, device="cuda")
+    with pytest.raises(ra.RAError) as e:  # D = 64 has no e4m3 kernel
+        ra.forward_fp8(q, q, q, 1.0, 1.0, 1.0, N=1)
+    assert e.value.status == -2
+    q = torch.zeros((1, 1, 256, 128), dtype=torch.float8_e4m3fn, device="cuda")
+    with pytest.raises(ra.RAError) as e:
+        ra.forward_fp8(q, q, q, 0.0, 1.0, 1.0, N=1)
+    assert e.value.status == -1
+    with pytest.raises(ra.RAError) as e:  # the plain entry point needs scales for e4m3
+        ra.forward(q, q, q, N=1)
+    assert e.value.status == -2
