@@ -49,6 +49,41 @@ def parse_args():
     return ap.parse_args()
 
 
+def rank_env():
+    """(world, rank, local_rank) from the launcher's environment (torchrun sets all three)."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_seed(w, rank):
+    """Every rank draws its own batch: replicas do not time identical inputs."""
+    return w.seed + rank
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    """The slowest rank's time: one all-reduce (MAX) of a float64 scalar, placed
+    where the process group's backend wants it (CUDA for nccl, host for gloo)."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world, step_flops, ms):
+    """Weak scaling: every rank runs one step of step_flops; the job's value is
+    the work of all ranks over the slowest rank's step time."""
+    return world * step_flops / (ms * 1e-3) / 1e12
+
+
 def flops_of(w, backward=None):
     fwd = 4.0 * w.B * w.H * w.S * w.S * w.D * (0.5 if w.causal else 1.0)
     bwd = 2.5 * fwd if (w.backward if backward is None else backward) else 0.0
@@ -192,7 +227,7 @@ def oracle_sample(w, budget_s, head=0):
 
 
 def run_reference(args, w):
-    rank = int(os.environ.get("RANK", "0"))
+    _, rank, _ = rank_env()
     if rank != 0:
         return
     per_step = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
@@ -385,9 +420,7 @@ def run_ours(args, w):
     import context_ra_forward_gb300 as ra
     from context_ra_forward_gb300 import inputs
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local_rank = rank_env()
     if world > 1:
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
@@ -395,20 +428,7 @@ def run_ours(args, w):
     dev = torch.device("cuda", torch.cuda.current_device())
     ra.lib()
 
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-
-    def max_over_ranks(x):
-        if world == 1:
-            return x
-        import torch.distributed as dist
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
-    host = inputs.make_inputs(w, seed=w.seed + rank)  # every rank: its own batch
+    host = inputs.make_inputs(w, seed=rank_seed(w, rank))
     path = Path(w, dev, host)
     fwd_fl, bwd_fl = flops_of(w)
     step_flops = fwd_fl + bwd_fl
@@ -420,7 +440,7 @@ def run_ours(args, w):
     if st != 0:
         raise RuntimeError(f"device status {st} {detail} after warm-up")
 
-    barrier()
+    barrier(world)
     torch.cuda.synchronize()
     sampler = ClockSampler(physical_gpu_index(local_rank)) if rank == 0 else None
     time.sleep(0.3 if sampler else 0.0)
@@ -432,17 +452,17 @@ def run_ours(args, w):
         path.step(events)
     t_end.record()
     torch.cuda.synchronize()
-    barrier()
+    barrier(world)
     launches = ra.kernel_launch_count() - launches0
     clocks = sampler.stop() if sampler else None
     ms = t_start.elapsed_time(t_end) / args.steps
-    ms = max_over_ranks(ms)
+    ms = max_over_ranks(ms, world)
     path.collect(events)
     st, detail = ra.check_device_status()
     if st != 0:
         raise RuntimeError(f"device status {st} {detail} after the timed region")
 
-    value = world * step_flops / (ms * 1e-3) / 1e12
+    value = whole_job_tflops(world, step_flops, ms)
 
     # dominant kernel: the phase with the largest share of the step
     phase = {p: path.phase_ms[p] / args.steps for p in Path.PHASES}
@@ -469,7 +489,7 @@ def run_ours(args, w):
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(path, w, args, step_flops, world, max_over_ranks)
+        e2e = run_e2e(path, w, args, step_flops, world)
 
     side = {}
     if not args.no_side_configs and rank == 0:
@@ -503,7 +523,7 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
-def run_e2e(path, w, args, step_flops, world, max_over_ranks):
+def run_e2e(path, w, args, step_flops, world):
     """Same step through the public API with HOST buffers: pinned-host inputs are
     copied in and the results copied out inside the timed region."""
     host_in = {n: torch.empty(path.x[n].shape, dtype=path.x[n].dtype, pin_memory=True) for n in path.names}
@@ -530,8 +550,8 @@ def run_e2e(path, w, args, step_flops, world, max_over_ranks):
         one()
     e1.record()
     torch.cuda.synchronize()
-    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
-    return {"value": round(world * step_flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    return {"value": round(whole_job_tflops(world, step_flops, ms), 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
