@@ -10,3 +10,4 @@ from .attention import (  # noqa: F401
     backward_dq_rows, backward_dkdv_cols, lse_merge, ring_forward,
     online_softmax_rows,
 )
+from .rope import rope_frequencies, rope_rotate  # noqa: F401

@@ -8,7 +8,7 @@ copies of the oracle and require that every planted mistake is caught.
 Pages cited:
   [CP]  "百万Token上下文训练的挑战与突破" §2.1 (contiguous split), §3.1 (ring)
   [ZZ]  "大模型如何訓練百萬 Token 上下文：上下文并行與 Ring Attention" §Zig Zag Ring Attention
-  [LC]  "超长上下文技术" survey §2.1.2 (ALiBi), §3.1.2 (online softmax)
+  [LC]  "超长上下文技术" survey §2.1.2 (ALiBi), §2.1.3 (RoPE), §3.1.2 (online softmax)
 """
 from __future__ import annotations
 
@@ -392,10 +392,82 @@ def pin_backward_partial(ora):
         assert np.max(np.abs(dvc - dv[:, :, cols])) < 1e-12
 
 
+# ---------------------------------------------------------------------------
+# RoPE ([LC] §2.1.3)
+# ---------------------------------------------------------------------------
+def pin_rope_frequencies(ora):
+    """theta_i = 1 / 10000^(2i/D): at D = 8 the four frequencies are 1, 1/10,
+    1/100, 1/1000; at D = 128 the same values sit at i = 0, 16, 32, 48."""
+    assert np.allclose(ora.rope_frequencies(8), [1.0, 0.1, 0.01, 0.001], rtol=1e-15, atol=0)
+    f = ora.rope_frequencies(128)
+    assert f.shape == (64,)
+    assert np.allclose(f[[0, 16, 32, 48]], [1.0, 0.1, 0.01, 0.001], rtol=1e-15, atol=0)
+    assert np.all(np.diff(f) < 0)
+
+
+def pin_rope_unit_vectors(ora):
+    """Closed form of the rotate-half formula on unit vectors, D = 8, with the
+    frequencies written out: e_j (j < 4) goes to cos(t w_j) e_j + sin(t w_j) e_{j+4};
+    e_{j+4} goes to -sin(t w_j) e_j + cos(t w_j) e_{j+4}."""
+    w = [1.0, 0.1, 0.01, 0.001]
+    pos = np.array([0, 1, 3, 7, 1000, 123457, 262143], dtype=np.float64)
+    for j in range(8):
+        x = np.zeros((len(pos), 8))
+        x[:, j] = 1.0
+        y = ora.rope_rotate(x, pos)
+        i = j % 4
+        want = np.zeros((len(pos), 8))
+        for n, t in enumerate(pos):
+            c, s = math.cos(t * w[i]), math.sin(t * w[i])
+            if j < 4:
+                want[n, i], want[n, i + 4] = c, s
+            else:
+                want[n, i], want[n, i + 4] = -s, c
+        assert np.max(np.abs(y - want)) < 1e-9, (j, np.max(np.abs(y - want)))
+
+
+def pin_rope_relative_position(ora):
+    """The page's claim: the rotation encodes relative position.  The score
+    <R(a) q, R(b) k> depends only on b - a: shifting both positions leaves it
+    unchanged, and it equals <q, R(b - a) k>."""
+    r = _rng(91)
+    S, D = 40, 16
+    q, k = r.standard_normal((S, D)), r.standard_normal((S, D))
+    pos = r.integers(0, 5000, size=S).astype(np.float64)
+    base = ora.rope_rotate(q, pos) @ ora.rope_rotate(k, pos).T
+    for shift in (1.0, 37.0, 100000.0):
+        got = ora.rope_rotate(q, pos + shift) @ ora.rope_rotate(k, pos + shift).T
+        assert np.max(np.abs(got - base)) < 1e-9
+    for a in range(0, S, 7):
+        rel = ora.rope_rotate(k, pos - pos[a]) @ q[a]
+        assert np.max(np.abs(rel - base[a])) < 1e-9
+
+
+def pin_rope_orthogonal(ora):
+    """A rotation: position 0 is the identity, each pair (i, i + D/2) keeps its
+    length, the inverse undoes it, and rotations by a then b compose to a + b."""
+    r = _rng(92)
+    x = r.standard_normal((2, 3, 33, 64))
+    pos = r.integers(0, 300000, size=33).astype(np.float64)
+    assert np.array_equal(ora.rope_rotate(x, np.zeros(33)), x)
+    y = ora.rope_rotate(x, pos)
+    pair = lambda z: z[..., :32] ** 2 + z[..., 32:] ** 2  # noqa: E731
+    assert np.max(np.abs(pair(y) - pair(x))) < 1e-10
+    assert np.max(np.abs(ora.rope_rotate(y, pos, inverse=True) - x)) < 1e-10
+    p2 = r.integers(0, 1000, size=33).astype(np.float64)
+    assert np.max(np.abs(ora.rope_rotate(y, p2) - ora.rope_rotate(x, pos + p2))) < 1e-9
+    # the inverse is the transpose: <R x, z> = <x, R^T z>
+    z = r.standard_normal(x.shape)
+    lhs = np.sum(y * z, axis=-1)
+    rhs = np.sum(x * ora.rope_rotate(z, pos, inverse=True), axis=-1)
+    assert np.max(np.abs(lhs - rhs)) < 1e-10
+
+
 ALL_PINS = [
     pin_index_golden, pin_index_bijection, pin_balance, pin_torch_forward,
     pin_brute_force, pin_rows_sum_to_one, pin_equal_keys, pin_alibi_zero_query,
     pin_shift_invariance, pin_merge_any_order, pin_ring_forward,
     pin_online_recurrence, pin_torch_backward, pin_backward_invariants,
-    pin_backward_partial,
+    pin_backward_partial, pin_rope_frequencies, pin_rope_unit_vectors,
+    pin_rope_relative_position, pin_rope_orthogonal,
 ]

@@ -12,8 +12,8 @@ import pytest
 
 from oracle_pins import ALL_PINS
 
-SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
-                   "oracle", "attention.py")
+ORACLE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle")
+SOURCES = ("attention.py", "rope.py")  # executed in this order into one mutant module
 
 MUTATIONS = {
     "dropped_scale": ("s = scale * (qrows @ k[keys].T)", "s = (qrows @ k[keys].T)"),
@@ -36,22 +36,34 @@ MUTATIONS = {
     "ring_direction_skips": ("steps = [(r - t) % N for t in range(N)]", "steps = [(r - t) % N for t in range(1, N)]"),
     "pairs_off_by_one": ("int(sum(g + 1 for g in shard))", "int(sum(g for g in shard))"),
     "strided_blocks": ("shards[g % N].append(g)", "shards[g // (S // N)].append(g)"),
+    # RoPE (rope.py)
+    "rope_interleaved_pairs": ("rope.py", "x1, x2 = x[..., :half], x[..., half:]",
+                               "x1, x2 = x[..., 0::2], x[..., 1::2]"),
+    "rope_exponent_halved": ("rope.py", "even = np.arange(0, D, 2, dtype=np.float64)",
+                             "even = np.arange(0, D // 2, dtype=np.float64)"),
+    "rope_rotation_sign": ("rope.py", "[x1 * c - x2 * s, x1 * s + x2 * c]", "[x1 * c + x2 * s, -x1 * s + x2 * c]"),
+    "rope_inverse_ignored": ("rope.py", "angle = -angle", "angle = angle"),
+    "rope_dropped_cos": ("rope.py", "x1 * s + x2 * c]", "x1 * s + x2]"),
 }
 
 
-def _load_mutant(name, old, new):
-    with open(SRC) as f:
-        text = f.read()
-    assert text.count(old) == 1, f"mutation {name}: anchor not found exactly once"
+def _load_mutant(name, target, old, new):
     mod = types.ModuleType(f"oracle_mutant_{name}")
-    exec(compile(text.replace(old, new), f"<mutant {name}>", "exec"), mod.__dict__)
+    for src in SOURCES:
+        with open(os.path.join(ORACLE, src)) as f:
+            text = f.read()
+        if src == target:
+            assert text.count(old) == 1, f"mutation {name}: anchor not found exactly once"
+            text = text.replace(old, new)
+        exec(compile(text, f"<mutant {name}: {src}>", "exec"), mod.__dict__)
     return mod
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
 def test_planted_mistake_is_caught(name):
-    old, new = MUTATIONS[name]
-    mod = _load_mutant(name, old, new)
+    spec = MUTATIONS[name]
+    target, old, new = spec if len(spec) == 3 else ("attention.py",) + spec
+    mod = _load_mutant(name, target, old, new)
     caught = []
     for pin in ALL_PINS:
         try:
