@@ -370,6 +370,39 @@ def fp8_config(cfg, dev, iters=3):
     return {"dtype": "e4m3", "forward_ms": round(ms, 3), "forward_tflops": round(fwd / ms / 1e9, 1)}
 
 
+def rope_config(cfg, dev, iters=10):
+    """The fused RoPE prologue (ra_rope_permute) on one tensor of the workload's
+    size, beside the plain permute it replaces: HBM-bound, read + write once
+    (each tensor is larger than L2, so no flush is needed between launches)."""
+    import context_ra_forward_gb300 as ra
+    from context_ra_forward_gb300 import inputs
+    w = inputs.WORKLOADS[cfg]
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed)
+    x = torch.randn((w.B, w.H, w.S, w.D), generator=g, device=dev).to(torch.bfloat16)
+    y = torch.empty_like(x)
+    nbytes = 2 * x.numel() * x.element_size()
+    peak = measured_peaks()[0].get("hbm_gbs")
+    res = {}
+    for name, call in (("rope_permute", lambda: ra.rope_permute(x, w.N, w.layout, out=y)),
+                       ("rope_unpermute", lambda: ra.rope_unpermute(x, w.N, w.layout, out=y)),
+                       ("permute", lambda: ra.zigzag_permute(x, w.N, w.layout, out=y))):
+        call()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(iters):
+            call()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / iters
+        gbs = nbytes / ms / 1e6
+        res[name] = {"ms": round(ms, 4), "GB_s": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak, 4)
+                     if peak else None}
+    res["bytes_per_launch"] = nbytes
+    return res
+
+
 def partials_config(cfg, dev, iters=2):
     """The separate-partials dataflow of a multi-device ring on one GPU: N ring-step
     launches writing fp32 partials plus N-1 LSE merges, against the same useful
@@ -499,6 +532,7 @@ def run_ours(args, w):
         side["C3_separate_partials"] = partials_config("C3", dev)
         side["C2_fp8"] = fp8_config("C2", dev)
         side["C3_fp8"] = fp8_config("C3", dev)
+        side["C5_rope"] = rope_config("C5", dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

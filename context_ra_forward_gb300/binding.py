@@ -47,6 +47,9 @@ def lib() -> ctypes.CDLL:
     L.ra_index_map.argtypes = [_i64, _i32, _i32, _vp, _vp]
     L.ra_zigzag_permute.argtypes = perm
     L.ra_unpermute.argtypes = perm
+    rope = [_vp, _vp, _i64, _i64, _i64, _i64, _i32, _i32, _i32, ctypes.c_double, _i64, _vp]
+    L.ra_rope_permute.argtypes = rope
+    L.ra_rope_unpermute.argtypes = rope
     L.ra_forward.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32, _i32, _vp,
                              _f32, _i32, _i32, _vp]
     L.ra_backward_workspace_bytes.argtypes = [_i64, _i64, _i64, _i64]
@@ -141,6 +144,29 @@ def zigzag_permute(x, N: int, layout: str = "zigzag", out=None, stream=None):
 def unpermute(x, N: int, layout: str = "zigzag", out=None, stream=None):
     """Shard-major order -> original order (ra_unpermute)."""
     return _permute(lib().ra_unpermute, x, N, layout, out, stream)
+
+
+def _rope(fn, x, N, layout, base, pos0, out, stream):
+    B, H, S, D = _bhsd(x, "x")
+    y = torch.empty_like(x) if out is None else out
+    _bhsd(y, "out")
+    if y.shape != x.shape or y.dtype != x.dtype:
+        raise ValueError("out must match x in shape and dtype")
+    _check(fn(_ptr(x), _ptr(y), B, H, S, D, DTYPES[x.dtype], N, _layout(layout), float(base), int(pos0),
+              _stream(stream)), fn.__name__)
+    return y
+
+
+def rope_permute(x, N: int, layout: str = "zigzag", *, base: float = 10000.0, pos0: int = 0, out=None,
+                 stream=None):
+    """RoPE at each row's global position, fused with original -> shard-major (ra_rope_permute)."""
+    return _rope(lib().ra_rope_permute, x, N, layout, base, pos0, out, stream)
+
+
+def rope_unpermute(x, N: int, layout: str = "zigzag", *, base: float = 10000.0, pos0: int = 0, out=None,
+                   stream=None):
+    """The transpose: shard-major -> original with the inverse rotation (ra_rope_unpermute)."""
+    return _rope(lib().ra_rope_unpermute, x, N, layout, base, pos0, out, stream)
 
 
 def forward_path(B, H, S, D, dtype, N, layout) -> int:

@@ -92,6 +92,30 @@ ra_status permute_common(const void* x, void* y, int64_t B, int64_t H, int64_t S
                                       static_cast<cudaStream_t>(stream)));
 }
 
+ra_status rope_common(const void* x, void* y, int64_t B, int64_t H, int64_t S, int64_t D, ra_dtype dt,
+                      int32_t N, ra_layout layout, double base, int64_t pos0, void* stream, bool inverse) {
+  ra_status s = check_sizes(B, H, S, D, dt, N, layout);
+  if (s != RA_OK) return s;
+  if (dt == RA_E4M3) return RA_ERR_UNSUPPORTED;
+  if (!(base > 1.0) || !isfinite(base)) return RA_ERR_INVALID_ARG;
+  if (pos0 < 0 || pos0 + S > (int64_t(1) << 31)) return RA_ERR_INVALID_ARG;
+  if (B == 0 || H == 0 || S == 0) return RA_OK;
+  if (!x || !y) return RA_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y, 16)) return RA_ERR_MISALIGNED;
+  if (overlaps(x, y, (size_t)(B * H * S * D * elem_bytes(dt)))) return RA_ERR_INVALID_ARG;
+  // theta_i / (2 pi) as a 64-bit binary fraction: below 1/(2 pi) since base > 1
+  ra::RopeTurns turns;
+  memset(&turns, 0, sizeof(turns));
+  const double inv_two_pi = 0.15915494309189535;
+  for (int64_t i = 0; i < D / 2; ++i) {
+    const double theta = 1.0 / pow(base, (double)(2 * i) / (double)D);
+    turns.f[i] = (uint64_t)llrint(ldexp(theta * inv_two_pi, 64));
+  }
+  const ra::SeqMap m = ra::SeqMap::make(S, N, layout);
+  return from_cuda(ra::launch_rope_permute(x, y, B, H, S, D, dt, m, inverse, pos0, turns,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
 bool is_sm103() {
   int dev = 0, major = 0, minor = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
@@ -177,6 +201,17 @@ ra_status ra_zigzag_permute(const void* x, void* y, int64_t B, int64_t H, int64_
 ra_status ra_unpermute(const void* x, void* y, int64_t B, int64_t H, int64_t S, int64_t D,
                        ra_dtype dt, int32_t N, ra_layout layout, void* stream) {
   return permute_common(x, y, B, H, S, D, dt, N, layout, stream, true);
+}
+
+ra_status ra_rope_permute(const void* x, void* y, int64_t B, int64_t H, int64_t S, int64_t D,
+                          ra_dtype dt, int32_t N, ra_layout layout, double base, int64_t pos0, void* stream) {
+  return rope_common(x, y, B, H, S, D, dt, N, layout, base, pos0, stream, false);
+}
+
+ra_status ra_rope_unpermute(const void* x, void* y, int64_t B, int64_t H, int64_t S, int64_t D,
+                            ra_dtype dt, int32_t N, ra_layout layout, double base, int64_t pos0,
+                            void* stream) {
+  return rope_common(x, y, B, H, S, D, dt, N, layout, base, pos0, stream, true);
 }
 
 int32_t ra_forward_path(int64_t B, int64_t H, int64_t S, int64_t D, ra_dtype dt, int32_t N,

@@ -33,6 +33,17 @@ void note_launch();
 cudaError_t launch_permute(const void* x, void* y, int64_t BH, int64_t S, int64_t row_bytes,
                            const SeqMap& m, bool inverse, cudaStream_t st);
 
+// ra_permute.cu — the same map with a rotary position embedding applied on the way.
+// F_i = theta_i / (2 pi) as a 64-bit binary fraction (turns per position), i < D/2.
+struct RopeTurns {
+  uint64_t f[128];
+};
+// inverse = false: y[slot] = R(pos0 + g(slot)) x[g(slot)]   (original -> shard-major)
+// inverse = true:  y[g] = R(pos0 + g)^T x[inv(g)]            (shard-major -> original)
+cudaError_t launch_rope_permute(const void* x, void* y, int64_t B, int64_t H, int64_t S, int64_t D,
+                                int32_t dtype, const SeqMap& m, bool inverse, int64_t pos0,
+                                const RopeTurns& turns, cudaStream_t st);
+
 // ra_simt.cu — CUDA-core kernels (exact fp32 arithmetic)
 cudaError_t launch_fwd_simt(const AttnArgs& a, void* o, float* lse, cudaStream_t st);
 // D_i = dO_i . O_i into dvec; also zeroes dq_acc ([B,H,S,D] fp32) when it is not null.

@@ -101,6 +101,42 @@ ra_status ra_unpermute(const void* x, void* y, int64_t B, int64_t H, int64_t S,
                        void* stream);
 
 /*
+ * ra_rope_permute — rotary position embedding fused with the permute:
+ *   y[b,h,p,:] = R(pos0 + g) x[b,h,g,:],  g = perm(p)   (original -> shard-major).
+ * [LC] §2.1.3 RoPE: the position enters Q and K through a rotation.  For a row at
+ * position t and each i in [0, D/2), with theta_i = 1 / base^(2i/D):
+ *   y[i]       = x[i] cos(t theta_i) - x[i + D/2] sin(t theta_i)
+ *   y[i + D/2] = x[i] sin(t theta_i) + x[i + D/2] cos(t theta_i)
+ * The position is the row's GLOBAL index g in the original sequence plus pos0
+ * (pos0 = 0 for a sequence that starts at position 0), so every shard's rows are
+ * rotated by their true positions whatever the layout.  Apply it to Q and K (not V,
+ * not dO) in place of ra_zigzag_permute.
+ *   x: device [B,H,S,D] `dtype`, original order; y: device, same shape, shard-major.
+ *   dtype: RA_F32 or RA_BF16 (the rotation runs in fp32, y is rounded once).
+ *   base: > 1 (the page's value is 10000).  pos0 >= 0 with pos0 + S <= 2^31.
+ * The angle t * theta_i is reduced to a fraction of a turn exactly (64-bit
+ * fixed-point turns per position): cos and sin carry an absolute error of a few
+ * 1e-7 at every position, not the 2^-6 rad an fp32 angle product reaches at 2^18.
+ * Errors: as ra_zigzag_permute; RA_ERR_UNSUPPORTED for RA_E4M3; RA_ERR_INVALID_ARG
+ * for base <= 1 or not finite, pos0 out of range, x and y overlapping.
+ */
+ra_status ra_rope_permute(const void* x, void* y, int64_t B, int64_t H, int64_t S,
+                          int64_t D, ra_dtype dtype, int32_t N, ra_layout layout,
+                          double base, int64_t pos0, void* stream);
+
+/*
+ * ra_rope_unpermute — the transpose of ra_rope_permute:
+ *   y[b,h,g,:] = R(pos0 + g)^T x[b,h,inv(g),:]   (shard-major -> original).
+ * R^T is the rotation by the negated angle, so this is both the inverse of
+ * ra_rope_permute (up to rounding) and the map that takes the gradients dQ and dK
+ * of the rotated, shard-major Q and K back to gradients of the caller's original
+ * Q and K.  Same arguments, layout and errors as ra_rope_permute.
+ */
+ra_status ra_rope_unpermute(const void* x, void* y, int64_t B, int64_t H, int64_t S,
+                            int64_t D, ra_dtype dtype, int32_t N, ra_layout layout,
+                            double base, int64_t pos0, void* stream);
+
+/*
  * ra_forward — exact softmax attention over N virtual ring shards.
  * [ZZ] §Zig Zag (each shard's Q meets every K/V block in ring-step order: at step
  * t shard r meets the K/V of shard (r-t) mod N), [CP] §3.1, [LC] §3.1.2 (blockwise
