@@ -64,9 +64,15 @@ constexpr uint32_t kOffDS = kOffQ + 2 * kStageBytes;  // dS^T, 32 KB
 constexpr uint32_t kOffBar = kOffDS + kTileBytes;
 enum Bar {
   kBarKV = 0,
-  kBarQFull = 1,  // + stage
-  kBarDrainFull = 3,  // the dQ partial of a Q tile is staged in its Q/dO stage
-  kBarSFull = 4,
+  kBarQFull = 1,    // + stage: the Q half of the stage is loaded
+  kBarDOFull = 3,   // + stage: the dO half of the stage is loaded
+  // + stage: dQ columns 0..63 of a Q tile are staged over its Q half, 64..127 over
+  // its dO half.  One barrier per stage: the producer waits for tile i after it has
+  // refilled tile i-1's stage, and tile i+1 may finish before that; only tile i+2,
+  // which needs this stage refilled, could complete the next phase of the barrier.
+  kBarDrainQ = 5,
+  kBarDrainDO = 7,
+  kBarSFull = 9,
   kBarDPFull,
   kBarPReady,
   kBarDSReady,
@@ -262,7 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t cnt = 1;
-      if (i == kBarPReady || i == kBarDSReady || i == kBarDQEmpty || i == kBarDrainFull) cnt = 8;
+      if (i == kBarPReady || i == kBarDSReady || i == kBarDQEmpty) cnt = 8;
+      if (i == kBarDrainQ || i == kBarDrainQ + 1 || i == kBarDrainDO || i == kBarDrainDO + 1) cnt = 4;
       mbar_init(bar(i), cnt);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -290,35 +297,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tma_load_3d(sbase + kOffV + hf * kBoxBytes, &tm_v, hf * 64, (int32_t)kp0, z, bar(kBarKV));
       }
       // Stage s holds Q and dO of Q tile i (s = i & 1) and, once that tile's MMAs
-      // are done, its dQ partial: after the softmax warps have staged it, this warp
-      // adds it to the accumulator with one bulk reduce, then refills the stage.
+      // are done, its dQ partial: columns 0..63 over the Q half, 64..127 over the
+      // dO half.  Each half is added to the accumulator with its own bulk reduce
+      // as soon as the softmax warps have staged it, and refilled as soon as the
+      // reduce has read it: Q first, which the next S^T product needs before dO.
       QWalk<kStrided> walk;
       walk.init(&P, kg0, s0);
       QTile qt;
       int64_t stage_p0[2] = {0, 0};
       int loaded = 0;
-      auto load = [&](const QTile& t) {
-        const int st = loaded & 1;
-        const uint32_t dst = sbase + kOffQ + st * kStageBytes;
-        mbar_arrive_expect_tx(bar(kBarQFull + st), kStageBytes);
-        for (int hf = 0; hf < 2; ++hf) {
-          tc::tma_load_3d(dst + hf * kBoxBytes, &tm_q, hf * 64, (int32_t)t.p0, z, bar(kBarQFull + st));
-          tc::tma_load_3d(dst + kTileBytes + hf * kBoxBytes, &tm_do, hf * 64, (int32_t)t.p0, z,
-                          bar(kBarQFull + st));
-        }
-        stage_p0[st] = t.p0;
-        ++loaded;
+      auto load_half = [&](const CUtensorMap* tm, int st, uint32_t off, int b, int64_t p0) {
+        const uint32_t dst = sbase + kOffQ + st * kStageBytes + off;
+        mbar_arrive_expect_tx(bar(b + st), kTileBytes);
+        for (int hf = 0; hf < 2; ++hf)
+          tc::tma_load_3d(dst + hf * kBoxBytes, tm, hf * 64, (int32_t)p0, z, bar(b + st));
       };
-      for (int s = 0; s < 2 && walk.next(qt); ++s) load(qt);
+      for (int st = 0; st < 2 && walk.next(qt); ++st) {
+        load_half(&tm_q, st, 0, kBarQFull, qt.p0);
+        load_half(&tm_do, st, kTileBytes, kBarDOFull, qt.p0);
+        stage_p0[st] = qt.p0;
+        ++loaded;
+      }
       for (int i = 0; i < loaded; ++i) {
         const int st = i & 1;
-        if (!mbar_wait(bar(kBarDrainFull), i & 1, P.status, kKernBwdTc, kSiteBwd)) break;
-        for (int b = 0; b < 4; ++b)  // four 128-row x 32-column fp32 boxes
-          tc::tma_reduce_add_3d(&tm_dq, sbase + kOffQ + st * kStageBytes + b * kBoxBytes, 32 * b,
-                                (int32_t)stage_p0[st], z);
+        const uint32_t src = sbase + kOffQ + st * kStageBytes;
+        if (!mbar_wait(bar(kBarDrainQ + st), (i >> 1) & 1, P.status, kKernBwdTc, kSiteBwd)) break;
+        for (int b = 0; b < 2; ++b)  // 128-row x 32-column fp32 boxes
+          tc::tma_reduce_add_3d(&tm_dq, src + b * kBoxBytes, 32 * b, (int32_t)stage_p0[st], z);
         tc::bulk_commit();
-        tc::bulk_wait_read0();  // the stage may be overwritten from here on
-        if (walk.next(qt)) load(qt);
+        tc::bulk_wait_read0();  // the Q half may be overwritten from here on
+        const bool next = walk.next(qt);
+        if (next) load_half(&tm_q, st, 0, kBarQFull, qt.p0);
+        if (!mbar_wait(bar(kBarDrainDO + st), (i >> 1) & 1, P.status, kKernBwdTc, kSiteBwd)) break;
+        for (int b = 2; b < 4; ++b)
+          tc::tma_reduce_add_3d(&tm_dq, src + b * kBoxBytes, 32 * b, (int32_t)stage_p0[st], z);
+        tc::bulk_commit();
+        tc::bulk_wait_read0();
+        if (next) {
+          load_half(&tm_do, st, kTileBytes, kBarDOFull, qt.p0);
+          stage_p0[st] = qt.p0;
+          ++loaded;
+        }
       }
       tc::bulk_wait_all0();
       // Let every load this warp issued land before the CTA can exit.
@@ -326,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int back = 1; back <= 2 && back <= loaded; ++back) {
         const int ii = loaded - back;
         mbar_wait(bar(kBarQFull + (ii & 1)), (ii >> 1) & 1, P.status, kKernBwdTc, kSiteQFull);
+        mbar_wait(bar(kBarDOFull + (ii & 1)), (ii >> 1) & 1, P.status, kKernBwdTc, kSiteQFull);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -340,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(bar(kBarQFull + 0), 0, P.status, kKernBwdTc, kSiteQFull);
         if (ok) {
           tc::fence_after_sync();
-          const uint32_t qb = sbase + kOffQ, dob = qb + kTileBytes;
+          const uint32_t qb = sbase + kOffQ;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {  // S^T = K Q^T
             const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
@@ -348,6 +368,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                        kIdescKK, kk > 0);
           }
           tc::mma_commit(bar(kBarSFull));
+          ok = mbar_wait(bar(kBarDOFull + 0), 0, P.status, kKernBwdTc, kSiteQFull);
+        }
+        if (ok) {
+          tc::fence_after_sync();
+          const uint32_t dob = sbase + kOffQ + kTileBytes;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {  // dP^T = V dO^T
             const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
@@ -400,7 +425,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                      kIdescKK, kk > 0);
         }
         tc::mma_commit(bar(kBarSFull));
-        ok = mbar_wait(bar(kBarDQEmpty), i & 1, P.status, kKernBwdTc, kSiteODone);
+        ok = mbar_wait(bar(kBarDQEmpty), i & 1, P.status, kKernBwdTc, kSiteODone) &&
+             mbar_wait(bar(kBarDOFull + nst), ((i + 1) >> 1) & 1, P.status, kKernBwdTc, kSiteQFull);
         if (!ok) break;
         tc::fence_after_sync();
 #pragma unroll
@@ -540,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarDrainFull));
+      if (lane == 0) mbar_arrive(bar((h == 0 ? kBarDrainQ : kBarDrainDO) + (i & 1)));
       ++i;
     }
     // ------------------------------------------------------------- epilogue: dK (scaled), dV
