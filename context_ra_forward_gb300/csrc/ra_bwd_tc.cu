@@ -218,10 +218,24 @@ __device__ __forceinline__ void compute_p(uint32_t t_row, int h, const float* ls
     for (int u = 0; u < 8; ++u) lv[u] = __ldg(reinterpret_cast<const float4*>(lse_q + 32 * ci) + u);
     tc::tmem_wait_ld();
 #pragma unroll
-    for (int u = 0; u < 32; ++u) {
+    for (int u = 0; u < 32; u += 2) {
       const float l4[4] = {lv[u >> 2].x, lv[u >> 2].y, lv[u >> 2].z, lv[u >> 2].w};
-      const float lse2 = l4[u & 3] * kLog2e;
-      p[32 * ci + u] = prob<kKind>(__uint_as_float(r[u]), lse2, 64 * h + 32 * ci + u, 32 * ci + u, c);
+      if constexpr (kKind == kGeneral) {
+        p[32 * ci + u] = prob<kKind>(__uint_as_float(r[u]), l4[u & 3] * kLog2e, 64 * h + 32 * ci + u, 32 * ci + u, c);
+        p[32 * ci + u + 1] = prob<kKind>(__uint_as_float(r[u + 1]), l4[(u + 1) & 3] * kLog2e,
+                                         64 * h + 32 * ci + u + 1, 32 * ci + u + 1, c);
+      } else {
+        // exponent arguments of the column pair in packed fp32 pairs: s * c2 (+ ALiBi) - LSE * log2(e)
+        float2 off = tc::mul2(make_float2(l4[u & 3], l4[(u + 1) & 3]), make_float2(-kLog2e, -kLog2e));
+        if constexpr (kKind == kLinear)
+          off = tc::add2(off, tc::fma2(make_float2(c.lin_sl, c.lin_sl),
+                                       make_float2((float)(32 * ci + u), (float)(32 * ci + u + 1)),
+                                       make_float2(c.lin_base, c.lin_base)));
+        const float2 x = tc::fma2(make_float2(__uint_as_float(r[u]), __uint_as_float(r[u + 1])),
+                                  make_float2(c.c2, c.c2), off);
+        p[32 * ci + u] = tc::ex2(x.x);
+        p[32 * ci + u + 1] = tc::ex2(x.y);
+      }
     }
   }
   uint32_t pk[32];
@@ -519,10 +533,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 4; ++e) {
             const int u = 8 * c8 + 2 * e;
             const float d0[4] = {dvv[u >> 2].x, dvv[u >> 2].y, dvv[u >> 2].z, dvv[u >> 2].w};
-            const float da = d0[u & 3], db = d0[(u + 1) & 3];
-            const float a = p[32 * ci + u] * (__uint_as_float(r[u]) - da);
-            const float b = p[32 * ci + u + 1] * (__uint_as_float(r[u + 1]) - db);
-            w[e] = tc::pack_bf16(a, b);
+            // P o (dP - D) for the column pair, in packed fp32 pairs
+            const float2 diff = tc::fma2(make_float2(d0[u & 3], d0[(u + 1) & 3]), make_float2(-1.f, -1.f),
+                                         make_float2(__uint_as_float(r[u]), __uint_as_float(r[u + 1])));
+            const float2 ab = tc::mul2(make_float2(p[32 * ci + u], p[32 * ci + u + 1]), diff);
+            w[e] = tc::pack_bf16(ab.x, ab.y);
             dsk[16 * ci + 4 * c8 + e] = w[e];
           }
           const int chunk = 4 * ci + c8;  // 16-byte chunk within the 128-byte row

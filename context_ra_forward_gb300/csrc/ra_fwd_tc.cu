@@ -251,8 +251,10 @@ __device__ __forceinline__ float tile_max(uint32_t t_s, const RowCtx& c) {
     const float lb = fmaf(c.sl, (float)(32 * ch), c.base);
     tc::tmem_wait_ld();
 #pragma unroll
-    for (int u = 0; u < 32; ++u)
-      mx[u & 3] = fmaxf(mx[u & 3], tile_score<kKind>(32 * ch + u, __uint_as_float(r[u]), fmaf(c.sl, (float)u, lb), c));
+    for (int u = 0; u < 32; u += 2)
+      mx[(u >> 1) & 3] =
+          tc::max3(mx[(u >> 1) & 3], tile_score<kKind>(32 * ch + u, __uint_as_float(r[u]), fmaf(c.sl, (float)u, lb), c),
+                   tile_score<kKind>(32 * ch + u + 1, __uint_as_float(r[u + 1]), fmaf(c.sl, (float)(u + 1), lb), c));
   }
   const float m = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
   return kKind == kPlain ? m * c.c2 : m;
@@ -261,6 +263,7 @@ __device__ __forceinline__ float tile_max(uint32_t t_s, const RowCtx& c) {
 template <int kKind, bool kFp8>
 __device__ __forceinline__ float tile_probs(uint32_t t_s, float mu, const RowCtx& c) {
   float ls[4] = {0.f, 0.f, 0.f, 0.f};
+  float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // bf16 path: pairs of partial sums
   auto prob = [&](float s) -> float {
     if constexpr (kKind == kPlain) return tc::ex2(fmaf(s, c.c2, -mu));
     else return tc::ex2(s - mu);
@@ -278,11 +281,23 @@ __device__ __forceinline__ float tile_probs(uint32_t t_s, float mu, const RowCtx
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
           const int col = 64 * hf + 32 * ci + 2 * u;
-          const float la = fmaf(c.sl, (float)(32 * ci + 2 * u), lb);
-          const float lb1 = fmaf(c.sl, (float)(32 * ci + 2 * u + 1), lb);
-          const float pa = prob(tile_score<kKind>(col, __uint_as_float(r[2 * u]), la, c));
-          const float pb = prob(tile_score<kKind>(col + 1, __uint_as_float(r[2 * u + 1]), lb1, c));
-          ls[u & 3] += pa + pb;
+          float2 x;  // exponent arguments of the column pair, scaled to the log2 domain
+          if constexpr (kKind == kPlain) {
+            x = tc::fma2(make_float2(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1])),
+                         make_float2(c.c2, c.c2), make_float2(-mu, -mu));
+          } else if constexpr (kKind == kLinear) {
+            // raw * c2 + (ALiBi term of the column - mu)
+            const float2 lin = tc::fma2(make_float2(c.sl, c.sl),
+                                        make_float2((float)(32 * ci + 2 * u), (float)(32 * ci + 2 * u + 1)),
+                                        make_float2(lb - mu, lb - mu));
+            x = tc::fma2(make_float2(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1])),
+                         make_float2(c.c2, c.c2), lin);
+          } else {
+            x = make_float2(tile_score<kKind>(col, __uint_as_float(r[2 * u]), 0.f, c) - mu,
+                            tile_score<kKind>(col + 1, __uint_as_float(r[2 * u + 1]), 0.f, c) - mu);
+          }
+          const float pa = tc::ex2(x.x), pb = tc::ex2(x.y);
+          ls2[u & 1] = tc::add2(ls2[u & 1], make_float2(pa, pb));
           pk[16 * ci + u] = tc::pack_bf16(pa, pb);
         }
       }
@@ -315,6 +330,7 @@ __device__ __forceinline__ float tile_probs(uint32_t t_s, float mu, const RowCtx
       tc::tmem_st16(t_s + 16 * hf, pk);
     }
   }
+  if constexpr (!kFp8) return (ls2[0].x + ls2[1].x) + (ls2[0].y + ls2[1].y);
   return (ls[0] + ls[1]) + (ls[2] + ls[3]);
 }
 
