@@ -51,7 +51,11 @@ constexpr int kTileBytes = kBM * kD * 2;   // 32 KB
 constexpr int kBoxBytes = kTileBytes / 2;  // 16 KB
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;  // 3 warpgroups: softmax x2, then producer, MMA and two idle warps
+// Register split (setmaxnreg, per warpgroup): the block launches with 168 per
+// thread (65536 / 384, rounded down to 8); the third warpgroup gives back to 56
+// and the softmax warpgroups take 224: 2 x 128 x 224 + 128 x 56 = 64512 = 384 x 168.
+constexpr uint32_t kRegsSoftmax = 224, kRegsOther = 56;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDK = 256, kColDV = 384;
 
@@ -249,7 +253,7 @@ __device__ __forceinline__ void fence_async_smem() {
 }
 
 template <bool kStrided>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ BwdParams P) {
@@ -296,6 +300,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  if (warp >= 8)
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
+  else
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
 
   if (warp == kProducerWarp) {
     if (lane == 0) {
@@ -458,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_before_sync();
     }
     __syncwarp();
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------- softmax warps
     const int qd = warp & 3;   // TMEM lane quarter: K/V rows 32*qd ..
     const int h = warp >> 2;   // Q column half: 64*h ..
