@@ -44,6 +44,10 @@ def _compile(src: str, extra: list[str]) -> str:
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"nvcc failed for {src}:\n{res.stdout}\n{res.stderr}")
+    if "setmaxnreg' ignored" in res.stdout + res.stderr:
+        # a register split the kernel's design relies on would silently not happen
+        os.remove(obj)
+        raise RuntimeError(f"ptxas ignored a setmaxnreg in {src}:\n{res.stderr}")
     return obj
 
 

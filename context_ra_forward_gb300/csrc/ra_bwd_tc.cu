@@ -53,9 +53,10 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kThreads = 384;  // 3 warpgroups: softmax x2, then producer, MMA and two idle warps
 // Register split (setmaxnreg, per warpgroup): the block launches with 168 per
-// thread (65536 / 384, rounded down to 8); the third warpgroup gives back to 56
-// and the softmax warpgroups take 224: 2 x 128 x 224 + 128 x 56 = 64512 = 384 x 168.
-constexpr uint32_t kRegsSoftmax = 224, kRegsOther = 56;
+// thread (65536 / 384, rounded down to 8); the third warpgroup gives back to 104
+// and the softmax warpgroups take 200: 2 x 128 x 200 + 128 x 104 = 64512 = 384 x 168.
+// (The smallest split at which neither side spills.)
+constexpr uint32_t kRegsSoftmax = 200, kRegsOther = 104;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDK = 256, kColDV = 384;
 
@@ -84,6 +85,7 @@ enum Bar {
   kBarDQFull,
   kBarDQEmpty,
   kBarFinal,
+  kBarEpiDone,  // every softmax warp has finished reading TMEM (count 8)
   kNumBars
 };
 constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
@@ -213,14 +215,16 @@ __device__ __forceinline__ float prob(float s, float lse2, int col, int colh, co
 template <int kKind>
 __device__ __forceinline__ void compute_p(uint32_t t_row, int h, const float* lse_q, const ColCtx& c,
                                           float (&p)[64]) {
+  uint32_t rr[2][32];
+  tc::tmem_ld32(t_row + kColS + 64 * h, rr[0]);
+  tc::tmem_ld32(t_row + kColS + 64 * h + 32, rr[1]);
 #pragma unroll
   for (int ci = 0; ci < 2; ++ci) {
-    uint32_t r[32];
-    tc::tmem_ld32(t_row + kColS + 64 * h + 32 * ci, r);
+    const uint32_t (&r)[32] = rr[ci];
     float4 lv[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) lv[u] = __ldg(reinterpret_cast<const float4*>(lse_q + 32 * ci) + u);
-    tc::tmem_wait_ld();
+    if (ci == 0) tc::tmem_wait_ld();
 #pragma unroll
     for (int u = 0; u < 32; u += 2) {
       const float l4[4] = {lv[u >> 2].x, lv[u >> 2].y, lv[u >> 2].z, lv[u >> 2].w};
@@ -253,7 +257,7 @@ __device__ __forceinline__ void fence_async_smem() {
 }
 
 template <bool kStrided>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ BwdParams P) {
@@ -286,7 +290,7 @@ __global__ void __launch_bounds__(kThreads)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t cnt = 1;
-      if (i == kBarPReady || i == kBarDSReady || i == kBarDQEmpty) cnt = 8;
+      if (i == kBarPReady || i == kBarDSReady || i == kBarDQEmpty || i == kBarEpiDone) cnt = 8;
       if (i == kBarDrainQ || i == kBarDrainQ + 1 || i == kBarDrainDO || i == kBarDrainDO + 1) cnt = 4;
       mbar_init(bar(i), cnt);
     }
@@ -300,11 +304,11 @@ __global__ void __launch_bounds__(kThreads)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  if (warp >= 8)
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
-  else
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
-
+  // The roles never meet again after this point (each register budget holds for
+  // the rest of its warps' code): the MMA warp frees TMEM once the softmax warps
+  // have signalled the end of their TMEM reads.
+  if (warp >= 8) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
   if (warp == kProducerWarp) {
     if (lane == 0) {
       tc::tma_prefetch_desc(&tm_q);
@@ -466,7 +470,12 @@ __global__ void __launch_bounds__(kThreads)
       tc::fence_before_sync();
     }
     __syncwarp();
-  } else if (warp < 8) {
+    mbar_wait(bar(kBarEpiDone), 0, P.status, kKernBwdTc, kSiteODone);
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     // ------------------------------------------------------------- softmax warps
     const int qd = warp & 3;   // TMEM lane quarter: K/V rows 32*qd ..
     const int h = warp >> 2;   // Q column half: 64*h ..
@@ -526,14 +535,16 @@ __global__ void __launch_bounds__(kThreads)
       tc::fence_after_sync();
       const float* dv_q = dvec_bh + qt.p0 + 64 * h;
       uint32_t dsk[32];  // dS^T as bf16 pairs, for the dK product from TMEM
+      uint32_t rr[2][32];
+      tc::tmem_ld32(t_row + kColDP + 64 * h, rr[0]);
+      tc::tmem_ld32(t_row + kColDP + 64 * h + 32, rr[1]);
 #pragma unroll
       for (int ci = 0; ci < 2; ++ci) {
-        uint32_t r[32];
-        tc::tmem_ld32(t_row + kColDP + 64 * h + 32 * ci, r);
+        const uint32_t (&r)[32] = rr[ci];
         float4 dvv[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) dvv[u] = __ldg(reinterpret_cast<const float4*>(dv_q + 32 * ci) + u);
-        tc::tmem_wait_ld();
+        if (ci == 0) tc::tmem_wait_ld();
 #pragma unroll
         for (int c8 = 0; c8 < 4; ++c8) {  // four 16-byte chunks of 8 columns
           uint32_t w[4];
@@ -616,12 +627,8 @@ __global__ void __launch_bounds__(kThreads)
       }
     }
     tc::fence_before_sync();
-  }
-
-  __syncthreads();
-  if (warp == kMmaWarp) {
-    tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, kTmemCols);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(kBarEpiDone));
   }
 }
 
