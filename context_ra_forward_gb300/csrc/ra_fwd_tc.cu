@@ -50,7 +50,11 @@ constexpr int kD = 128;
 constexpr int kStages = 2;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;  // 3 warpgroups: softmax x2, then producer, MMA and two idle warps
+// Register split (setmaxnreg, per warpgroup): the block launches with 168 per
+// thread (65536 / 384, rounded down to 8); the third warpgroup gives back to 104
+// and the softmax warpgroups take 200: 2 x 128 x 200 + 128 x 104 = 64512 = 384 x 168.
+constexpr uint32_t kRegsSoftmax = 200, kRegsOther = 104;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;
 
@@ -64,7 +68,8 @@ enum Bar {
   kBarPFull = kBarSFull + 2,
   kBarODone = kBarPFull + 2,
   kBarFinal = kBarODone + 2,
-  kNumBars = kBarFinal + 1
+  kBarEpiDone = kBarFinal + 1,  // every softmax thread has finished reading TMEM
+  kNumBars = kBarEpiDone + 1
 };
 
 // Element-type dependent layout.  Shared-memory rows are 128 bytes either way
@@ -239,6 +244,64 @@ __device__ __forceinline__ float tile_score(int u, float raw, float lin, const R
   }
 }
 
+// kPlain tiles (the common case): the row's 128 scores are read from TMEM once
+// and both passes run from registers.  The other kinds keep the two rolled TMEM
+// passes (their per-element work would not fit beside 128 held scores).
+using SRow = uint32_t[4][32];
+
+__device__ __forceinline__ float plain_max(const SRow& sr, float c2) {
+  float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+    for (int u = 0; u < 32; u += 2)
+      mx[(u >> 1) & 3] = tc::max3(mx[(u >> 1) & 3], __uint_as_float(sr[ch][u]), __uint_as_float(sr[ch][u + 1]));
+  return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c2;
+}
+
+template <bool kFp8>
+__device__ __forceinline__ float plain_probs(uint32_t t_s, const SRow& sr, float mu, float c2) {
+  if constexpr (!kFp8) {
+    float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      uint32_t pk[32];
+#pragma unroll
+      for (int ci = 0; ci < 2; ++ci)
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const uint32_t* r = sr[2 * hf + ci];
+          const float2 x = tc::fma2(make_float2(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1])),
+                                    make_float2(c2, c2), make_float2(-mu, -mu));
+          const float pa = tc::ex2(x.x), pb = tc::ex2(x.y);
+          ls2[u & 1] = tc::add2(ls2[u & 1], make_float2(pa, pb));
+          pk[16 * ci + u] = tc::pack_bf16(pa, pb);
+        }
+      tc::tmem_st32(t_s + 32 * hf, pk);
+    }
+    return (ls2[0].x + ls2[1].x) + (ls2[0].y + ls2[1].y);
+  } else {
+    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      uint32_t pk[16];
+#pragma unroll
+      for (int ci = 0; ci < 2; ++ci)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t* r = sr[2 * hf + ci];
+          float pv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) pv[e] = tc::ex2(fmaf(__uint_as_float(r[4 * u + e]), c2, -mu));
+          ls[u & 3] += (pv[0] + pv[1]) + (pv[2] + pv[3]);
+          pk[8 * ci + u] = tc::pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
+        }
+      tc::tmem_st16(t_s + 16 * hf, pk);
+    }
+    return (ls[0] + ls[1]) + (ls[2] + ls[3]);
+  }
+}
+
 template <int kKind>
 __device__ __forceinline__ float tile_max(uint32_t t_s, const RowCtx& c) {
   float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -402,6 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t cnt = 1;
       if (i == kBarPFull || i == kBarPFull + 1) cnt = 128;
+      if (i == kBarEpiDone) cnt = 8;
       mbar_init(bar(i), cnt);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -415,6 +479,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
+  // The roles never meet again after this point (each register budget holds for
+  // the rest of its warps' code): the MMA warp frees TMEM once the softmax warps
+  // have signalled the end of their TMEM reads.
+  if (warp >= 8) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
   if (warp == kProducerWarp) {
     if (lane == 0) {
       tc::tma_prefetch_desc(&tm_q);
@@ -523,7 +592,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_before_sync();
     }
     __syncwarp();
+    mbar_wait(bar(kBarEpiDone), 0, P.status, kKernFwdTc, kSiteODone);
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     // ------------------------------------------------------------- softmax
     const int X = warp >> 2;
     const int wq = warp & 3;
@@ -586,33 +660,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       rc.row_ok = row_ok;
       rc.alibi = alibi;
       rc.gtab = gtab;
-      // Pass 1: the row max of this tile (log2 domain).
-      const float mt = kind == kPlain ? tile_max<kPlain>(t_s, rc)
-                                      : (kind == kLinear ? tile_max<kLinear>(t_s, rc) : tile_max<kGeneral>(t_s, rc));
-      // Move the reference max only when the tile's max exceeds it by > 8.
-      const bool need = mt > m_ref + kRescaleThreshold;
-      if (__any_sync(0xffffffffu, need)) {
-        const float m_new = need ? mt : m_ref;
-        const float alpha = need ? (m_ref == -INFINITY ? 0.f : tc::ex2(m_ref - m_new)) : 1.f;
-        if (j > 0) {
+      // Move the reference max only when the tile's max exceeds it by > 8; returns
+      // the offset the probabilities are taken against.
+      auto move_max = [&](float mt) -> float {
+        const bool need = mt > m_ref + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          const float m_new = need ? mt : m_ref;
+          const float alpha = need ? (m_ref == -INFINITY ? 0.f : tc::ex2(m_ref - m_new)) : 1.f;
+          if (j > 0) {
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];
-            tc::tmem_ld32(t_o + 32 * c, r);
-            tc::tmem_wait_ld();
+            for (int c = 0; c < 4; ++c) {
+              uint32_t r[32];
+              tc::tmem_ld32(t_o + 32 * c, r);
+              tc::tmem_wait_ld();
 #pragma unroll
-            for (int u = 0; u < 32; ++u) r[u] = __float_as_uint(__uint_as_float(r[u]) * alpha);
-            tc::tmem_st32(t_o + 32 * c, r);
+              for (int u = 0; u < 32; ++u) r[u] = __float_as_uint(__uint_as_float(r[u]) * alpha);
+              tc::tmem_st32(t_o + 32 * c, r);
+            }
           }
+          l *= alpha;
+          m_ref = m_new;
         }
-        l *= alpha;
-        m_ref = m_new;
+        return m_ref == -INFINITY ? 0.f : m_ref;
+      };
+      // Pass 1: the row max of this tile (log2 domain); pass 2: probabilities,
+      // packed to bf16 pairs and stored over S columns that have already been read
+      // (P column k holds scores 2k, 2k+1).
+      if (kind == kPlain) {
+        SRow sr;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) tc::tmem_ld32(t_s + 32 * ch, sr[ch]);
+        tc::tmem_wait_ld();
+        const float mu = move_max(plain_max(sr, c2));
+        l += plain_probs<kFp8>(t_s, sr, mu, c2);
+      } else if (kind == kLinear) {
+        const float mu = move_max(tile_max<kLinear>(t_s, rc));
+        l += tile_probs<kLinear, kFp8>(t_s, mu, rc);
+      } else {
+        const float mu = move_max(tile_max<kGeneral>(t_s, rc));
+        l += tile_probs<kGeneral, kFp8>(t_s, mu, rc);
       }
-      const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-      // Pass 2: probabilities, packed to bf16 pairs and stored over S columns that
-      // have already been read (P column k holds scores 2k, 2k+1).
-      l += kind == kPlain ? tile_probs<kPlain, kFp8>(t_s, mu, rc)
-                          : (kind == kLinear ? tile_probs<kLinear, kFp8>(t_s, mu, rc) : tile_probs<kGeneral, kFp8>(t_s, mu, rc));
       tc::tmem_wait_st();
       tc::fence_before_sync();
       mbar_arrive(bar(kBarPFull + X));
@@ -655,12 +742,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (row_ok) P.lse[bh * S + slot] = l != 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
     }
     tc::fence_before_sync();
-  }
-
-  __syncthreads();
-  if (warp == kMmaWarp) {
-    tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, kTmemCols);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(kBarEpiDone));
   }
 }
 
