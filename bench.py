@@ -410,6 +410,28 @@ def rope_config(cfg, dev, iters=10):
     return res
 
 
+def strided_step(cfg, dev, iters=2):
+    """The whole step (permute, forward, backward, unpermute) of the token-strided
+    layout at full size (context for the single line)."""
+    from context_ra_forward_gb300 import inputs
+    w = inputs.WORKLOADS[cfg]
+    path = Path(w, dev)
+    path.step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        path.step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / iters
+    fwd, bwd = flops_of(w)
+    res = {"layout": w.layout, "ms_per_step": round(ms, 3), "tflops": round((fwd + bwd) / ms / 1e9, 1)}
+    del path
+    torch.cuda.empty_cache()
+    return res
+
+
 def partials_config(cfg, dev, iters=2):
     """The separate-partials dataflow of a multi-device ring on one GPU: N ring-step
     launches writing fp32 partials plus N-1 LSE merges, against the same useful
@@ -540,6 +562,7 @@ def run_ours(args, w):
         side["C2_fp8"] = fp8_config("C2", dev)
         side["C3_fp8"] = fp8_config("C3", dev)
         side["C5_rope"] = rope_config("C5", dev)
+        side["C5S_step"] = strided_step("C5S", dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

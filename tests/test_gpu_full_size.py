@@ -43,7 +43,7 @@ def _sample_rows(w, count):
     return np.unique(np.concatenate([perm[slots], [0, w.S - 1]]))
 
 
-@pytest.mark.parametrize("cfg", ["C2", "C3", "C4", "C5"])
+@pytest.mark.parametrize("cfg", ["C2", "C3", "C4", "C5", "C3S", "C5S"])
 def test_full_size(cfg):
     w = inputs.WORKLOADS[cfg]
     x, res = _run(w)
