@@ -216,8 +216,7 @@ template <int kKind>
 __device__ __forceinline__ void compute_p(uint32_t t_row, int h, const float* lse_q, const ColCtx& c,
                                           float (&p)[64]) {
   uint32_t rr[2][32];
-  tc::tmem_ld32(t_row + kColS + 64 * h, rr[0]);
-  tc::tmem_ld32(t_row + kColS + 64 * h + 32, rr[1]);
+  tc::tmem_ld64(t_row + kColS + 64 * h, rr);
 #pragma unroll
   for (int ci = 0; ci < 2; ++ci) {
     const uint32_t (&r)[32] = rr[ci];
@@ -536,8 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* dv_q = dvec_bh + qt.p0 + 64 * h;
       uint32_t dsk[32];  // dS^T as bf16 pairs, for the dK product from TMEM
       uint32_t rr[2][32];
-      tc::tmem_ld32(t_row + kColDP + 64 * h, rr[0]);
-      tc::tmem_ld32(t_row + kColDP + 64 * h + 32, rr[1]);
+      tc::tmem_ld64(t_row + kColDP + 64 * h, rr);
 #pragma unroll
       for (int ci = 0; ci < 2; ++ci) {
         const uint32_t (&r)[32] = rr[ci];
@@ -580,10 +578,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc::fence_after_sync();
       {
-        uint32_t r0[32], r1[32];
-        tc::tmem_ld32(t_row + kColDP + 64 * h, r0);
-        tc::tmem_ld32(t_row + kColDP + 64 * h + 32, r1);
+        uint32_t rr[2][32];
+        tc::tmem_ld64(t_row + kColDP + 64 * h, rr);
         tc::tmem_wait_ld();
+        const uint32_t (&r0)[32] = rr[0];
+        const uint32_t (&r1)[32] = rr[1];
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarDQEmpty));

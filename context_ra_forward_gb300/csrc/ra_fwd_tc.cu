@@ -688,8 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (P column k holds scores 2k, 2k+1).
       if (kind == kPlain) {
         SRow sr;
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) tc::tmem_ld32(t_s + 32 * ch, sr[ch]);
+        tc::tmem_ld128(t_s, sr);
         tc::tmem_wait_ld();
         const float mu = move_max(plain_max(sr, c2));
         l += plain_probs<kFp8>(t_s, sr, mu, c2);
