@@ -92,3 +92,69 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError):
         binding.lib()
+
+
+def _p(x):
+    return ctypes.c_void_p(x)
+
+
+F0 = ctypes.c_float(0.0)
+
+
+def test_size_limits_rejected_before_launch(L):
+    """The documented limits: S*D*e/16 < 2^31 per head and B*H*S*D < 4e18."""
+    a, b, c, o = _p(1 << 20), _p(2 << 40), _p(3 << 40), _p(4 << 40)
+    lse = _p(5 << 40)
+    # S = 2^30 rows of D = 128 bf16: 2^34 16-byte chunks per head
+    assert L.ra_forward(a, b, c, o, lse, 1, 1, 1 << 30, 128, 1, 1, None, F0, 1, 0, None) == -2
+    assert L.ra_forward_path(1 << 20, 1 << 20, 1 << 20, 128, 1, 1, 0) == -2
+    assert L.ra_zigzag_permute(a, o, 1, 1, 1 << 30, 128, 1, 1, 0, None) == -2
+
+
+def test_rope_validation(L):
+    x, y = _p(1 << 20), _p(1 << 40)
+    rp = L.ra_rope_permute
+    assert rp(x, y, 1, 2, 64, 128, 1, 4, 1, 1.0, 0, None) == -1            # base must exceed 1
+    assert rp(x, y, 1, 2, 64, 128, 1, 4, 1, float("nan"), 0, None) == -1
+    assert rp(x, y, 1, 2, 64, 128, 1, 4, 1, 10000.0, -1, None) == -1       # negative position offset
+    assert rp(x, y, 1, 2, 64, 128, 1, 4, 1, 10000.0, (1 << 31) - 10, None) == -1  # past 2^31
+    assert rp(x, y, 1, 2, 64, 128, 2, 4, 1, 10000.0, 0, None) == -2        # e4m3
+    assert rp(x, y, 1, 2, 64, 96, 1, 4, 1, 10000.0, 0, None) == -2         # D
+    assert rp(None, None, 1, 2, 0, 128, 1, 4, 1, 10000.0, 0, None) == 0    # empty: no launch
+    assert rp(x, x, 1, 2, 64, 128, 1, 4, 1, 10000.0, 0, None) == -1        # in place
+    assert rp(_p(8), y, 1, 2, 64, 128, 1, 4, 1, 10000.0, 0, None) == -3    # misaligned
+    assert L.ra_rope_unpermute(x, y, 1, 2, 64, 128, 1, 4, 1, 0.5, 0, None) == -1
+
+
+def test_fp8_ring_step_and_merge_validation(L):
+    q, k, v, o, lse = (_p(n << 40) for n in range(1, 6))
+    f8 = L.ra_forward_fp8
+    one = ctypes.c_float(1.0)
+    assert f8(q, k, v, ctypes.c_float(0.0), one, one, o, lse, 1, 2, 256, 128, 1, None, F0, 2, 1, None) == -1
+    assert f8(q, k, v, one, ctypes.c_float(float("inf")), one, o, lse, 1, 2, 256, 128, 1, None, F0, 2, 1,
+              None) == -1
+    assert f8(q, k, v, one, one, one, o, lse, 1, 2, 256, 64, 1, None, F0, 2, 1, None) == -2  # D = 64
+    rs = L.ra_forward_ring_step
+    assert rs(q, k, v, o, lse, 1, 2, 2048, 128, 1, 1, None, F0, 4, 1, 4, None) == -1  # step == N
+    assert rs(q, k, v, o, lse, 1, 2, 2048, 128, 1, 1, None, F0, 4, 1, -1, None) == -1
+    assert rs(q, k, v, o, lse, 1, 2, 1024, 128, 1, 1, None, F0, 4, 1, 0, None) == -2  # runs of 128 rows
+    mg = L.ra_lse_merge
+    assert mg(q, k, v, o, None, 1, 1, 2, 64, 96, None) == -2              # D
+    assert mg(q, k, v, o, lse, 2, 1, 2, 64, 128, None) == -2              # e4m3 output
+    assert mg(None, None, None, None, None, 1, 1, 2, 0, 128, None) == 0   # empty
+    assert mg(q, k, q, o, None, 1, 1, 2, 64, 128, None) == -1             # accumulator aliases the partial
+
+
+def test_backward_validation(L):
+    ptrs = [_p(n << 40) for n in range(1, 10)]  # q k v o lse do dq dk dv
+    q, k, v, o, lse, do, dq, dk, dv = ptrs
+    bw = L.ra_backward
+    need = L.ra_backward_workspace_bytes(1, 2, 1024, 128)
+    ws = _p(20 << 40)
+    args = (1, 2, 1024, 128, 1, 1, None, F0, 4, 1, None)
+    assert bw(q, k, v, o, lse, do, dq, dk, dv, ws, need - 1, *args) == -6       # workspace too small
+    assert bw(q, k, v, o, lse, do, dq, dk, dv, None, need, *args) == -6
+    assert bw(q, k, v, o, lse, do, dq, dk, dv, _p((20 << 40) + 16), need, *args) == -3  # not 256-aligned
+    assert bw(q, k, v, o, lse, do, q, dk, dv, ws, need, *args) == -1            # dQ over Q
+    assert bw(q, k, v, o, lse, do, dq, dk, dk, ws, need, *args) == -1           # dK over dV
+    assert bw(q, k, v, o, lse, do, dq, dk, dv, ws, need, 1, 2, 1024, 128, 2, 1, None, F0, 4, 1, None) == -2
