@@ -290,9 +290,11 @@ __device__ __forceinline__ float plain_probs(uint32_t t_s, const SRow& sr, float
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           const uint32_t* r = sr[2 * hf + ci];
-          float pv[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) pv[e] = tc::ex2(fmaf(__uint_as_float(r[4 * u + e]), c2, -mu));
+          const float2 x0 = tc::fma2(make_float2(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1])),
+                                     make_float2(c2, c2), make_float2(-mu, -mu));
+          const float2 x1 = tc::fma2(make_float2(__uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3])),
+                                     make_float2(c2, c2), make_float2(-mu, -mu));
+          const float pv[4] = {tc::ex2(x0.x), tc::ex2(x0.y), tc::ex2(x1.x), tc::ex2(x1.y)};
           ls[u & 3] += (pv[0] + pv[1]) + (pv[2] + pv[3]);
           pk[8 * ci + u] = tc::pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
         }
