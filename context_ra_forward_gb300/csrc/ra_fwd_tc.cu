@@ -626,10 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int j = 0;
     bool ok = true;
     while (walk.next(tile)) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarSFull + X), j & 1, P.status, kKernFwdTc, kSiteSFull));
-      if (!ok) break;
-      tc::fence_after_sync();
-      // Classify the tile for this Q tile.
+      // Classify the tile for this Q tile (before waiting for its scores).
       const bool below = tile.gmax <= qgmin;              // every key at or before every query
       const bool above = !P.causal && tile.gmin >= qgmax; // every key at or after every query
       // kPlain: every key visible to every row, no bias; kLinear: the same with an
@@ -662,6 +659,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       rc.row_ok = row_ok;
       rc.alibi = alibi;
       rc.gtab = gtab;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarSFull + X), j & 1, P.status, kKernFwdTc, kSiteSFull));
+      if (!ok) break;
+      tc::fence_after_sync();
       // Move the reference max only when the tile's max exceeds it by > 8; returns
       // the offset the probabilities are taken against.
       auto move_max = [&](float mt) -> float {

@@ -21,6 +21,12 @@ CASES = [
     ("strided_alibi", "bf16", True, True, 4, "strided", 1, 2, 2048, 128),
     ("strided_nc_alibi", "bf16", False, True, 2, "strided", 1, 1, 1024, 128),
     ("strided_ragged", "bf16", True, False, 3, "strided", 1, 2, 1200, 128),
+    # several batches and heads (per-(b, h) block order, per-head ALiBi slopes)
+    ("batch_heads", "bf16", True, True, 2, "zigzag", 2, 3, 1024, 128),
+    ("batch_heads_nc", "bf16", False, False, 4, "contiguous", 3, 2, 512, 128),
+    # fp32 (CUDA-core path) with a ragged tail and a strided layout
+    ("f32_ragged", "f32", True, False, 3, "zigzag", 1, 2, 600, 64),
+    ("f32_strided", "f32", True, True, 4, "strided", 2, 1, 512, 128),
 ]
 
 
