@@ -213,17 +213,16 @@ __device__ __forceinline__ float prob(float s, float lse2, int col, int colh, co
 // P^T for this warp's 64 query columns: from S^T in TMEM into registers (fp32)
 // and back into TMEM as bf16 pairs for the dV product.
 template <int kKind>
-__device__ __forceinline__ void compute_p(uint32_t t_row, int h, const float* lse_q, const ColCtx& c,
+// lva: the 64 LSE values of these columns, loaded before S^T was waited for.
+__device__ __forceinline__ void compute_p(uint32_t t_row, int h, const float4 (&lva)[16], const ColCtx& c,
                                           float (&p)[64]) {
   uint32_t rr[2][32];
   tc::tmem_ld64(t_row + kColS + 64 * h, rr);
+  tc::tmem_wait_ld();
 #pragma unroll
   for (int ci = 0; ci < 2; ++ci) {
     const uint32_t (&r)[32] = rr[ci];
-    float4 lv[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) lv[u] = __ldg(reinterpret_cast<const float4*>(lse_q + 32 * ci) + u);
-    if (ci == 0) tc::tmem_wait_ld();
+    const float4* lv = lva + 8 * ci;
 #pragma unroll
     for (int u = 0; u < 32; u += 2) {
       const float l4[4] = {lv[u >> 2].x, lv[u >> 2].y, lv[u >> 2].z, lv[u >> 2].w};
@@ -514,14 +513,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       cc.lin_base = (below ? -slope2 * (float)(qt.g0 - gj) : -slope2 * (float)(gj - qt.g0)) +
                     cc.lin_sl * (float)(64 * h);  // this warp's first column
 
+      // this tile's LSE row is loaded while S^T is computed (and its D row while dP^T is)
+      float4 lva[16];
+      {
+        const float4* lse_q = reinterpret_cast<const float4*>(lse_bh + qt.p0 + 64 * h);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) lva[u] = __ldg(lse_q + u);
+      }
       ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarSFull), i & 1, P.status, kKernBwdTc, kSiteSFull));
       if (!ok) break;
       tc::fence_after_sync();
       float p[64];
-      const float* lse_q = lse_bh + qt.p0 + 64 * h;
-      if (kind == kPlain) compute_p<kPlain>(t_row, h, lse_q, cc, p);
-      else if (kind == kLinear) compute_p<kLinear>(t_row, h, lse_q, cc, p);
-      else compute_p<kGeneral>(t_row, h, lse_q, cc, p);
+      if (kind == kPlain) compute_p<kPlain>(t_row, h, lva, cc, p);
+      else if (kind == kLinear) compute_p<kLinear>(t_row, h, lva, cc, p);
+      else compute_p<kGeneral>(t_row, h, lva, cc, p);
       tc::tmem_wait_st();
       tc::fence_before_sync();
       __syncwarp();
