@@ -527,6 +527,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (kind == kPlain) compute_p<kPlain>(t_row, h, lva, cc, p);
       else if (kind == kLinear) compute_p<kLinear>(t_row, h, lva, cc, p);
       else compute_p<kGeneral>(t_row, h, lva, cc, p);
+      // the D row, loaded while dP^T is computed
+      float4 dva[16];
+      {
+        const float4* dv_q = reinterpret_cast<const float4*>(dvec_bh + qt.p0 + 64 * h);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) dva[u] = __ldg(dv_q + u);
+      }
       tc::tmem_wait_st();
       tc::fence_before_sync();
       __syncwarp();
@@ -537,17 +544,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        mbar_wait(bar(kBarDSFree), (i & 1) ^ 1, P.status, kKernBwdTc, kSiteBwd));
       if (!ok) break;
       tc::fence_after_sync();
-      const float* dv_q = dvec_bh + qt.p0 + 64 * h;
       uint32_t dsk[32];  // dS^T as bf16 pairs, for the dK product from TMEM
-      uint32_t rr[2][32];
-      tc::tmem_ld64(t_row + kColDP + 64 * h, rr);
 #pragma unroll
       for (int ci = 0; ci < 2; ++ci) {
-        const uint32_t (&r)[32] = rr[ci];
-        float4 dvv[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) dvv[u] = __ldg(reinterpret_cast<const float4*>(dv_q + 32 * ci) + u);
-        if (ci == 0) tc::tmem_wait_ld();
+        uint32_t r[32];
+        tc::tmem_ld32(t_row + kColDP + 64 * h + 32 * ci, r);
+        tc::tmem_wait_ld();
+        const float4* dvv = dva + 8 * ci;
 #pragma unroll
         for (int c8 = 0; c8 < 4; ++c8) {  // four 16-byte chunks of 8 columns
           uint32_t w[4];
