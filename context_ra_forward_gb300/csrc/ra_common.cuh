@@ -28,6 +28,8 @@ enum KernelId : int32_t { kKernFwdTc = 1, kKernBwdTc = 2, kKernDebug = 3 };
 // Limit of every in-kernel wait (nanoseconds of %globaltimer).  Work between two
 // waits is one tile (microseconds), so two seconds only expires on a lost signal.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// Below this a wait does not look at the status word (see mbar_wait).
+constexpr uint64_t kStatusCheckNs = 50000ull;
 
 // ----------------------------------------------------------------------------
 // Sequence -> shard-major slot maps ([CP] §2.1, [ZZ] §Zig Zag)
@@ -189,11 +191,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
+    // The status word (a global load, slow under load) is consulted only once a
+    // wait has lasted longer than any wait of a healthy pipeline, so that an
+    // ordinary wait wakes as soon as its phase completes.
+    const uint64_t dt = globaltimer_ns() - t0;
+    if (dt < kStatusCheckNs) continue;
     if (status != nullptr && *reinterpret_cast<volatile int32_t*>(status) != 0) {
       record_wait_site(status, bar, parity, site);
       return false;
     }
-    if (globaltimer_ns() - t0 > limit_ns) {
+    if (dt > limit_ns) {
       record_failure(status, RA_ERR_TIMEOUT, kernel, site);
       record_wait_site(status, bar, parity, site);
       return false;
