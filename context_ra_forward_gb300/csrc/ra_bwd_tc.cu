@@ -14,12 +14,13 @@
 // tiles that see it in ring order (the queries of shard (s + t) mod N at step t),
 // skipping tiles every query of which lies before every key (causal).
 //
-// Warp roles (320 threads):
+// Warp roles (384 threads, three warpgroups; setmaxnreg gives the two softmax
+// warpgroups 200 registers and the third 104):
 //   warps 0-7  "softmax": warp w owns K/V rows 32*(w%4).. (its TMEM lane quarter)
 //              and Q columns 64*(w/4)..: P^T, dS^T, the dQ drain, the dK/dV epilogue
 //   warp  8    TMA producer: K and V once, then Q and dO tiles into a 2-stage ring;
-//              it also issues the bulk reduce-add of each Q tile's dQ partial
-//   warp  9    TMEM allocation and MMA issue (one thread)
+//              it also issues the bulk reduce-adds of each Q tile's dQ partial
+//   warp  9    TMEM allocation and MMA issue (one thread); warps 10-11 idle
 // TMEM (512 columns): S^T [0,128), dP^T [128,256), dK [256,384), dV [384,512);
 // all fp32 with K/V row r in lane r.  P^T (bf16 pairs) is written back over S^T
 // (Q columns 0..63 -> TMEM columns 0..31, 64..127 -> 64..95), the dQ partial of
@@ -31,8 +32,11 @@
 // MMA order per Q tile i:  [P^T_i] dV_i  [dS^T_i] dK_i, dQ_i -> S^T_{i+1}
 //                          [dQ_i drained] dP^T_{i+1}.
 // dQ partials are staged in shared memory and added into an fp32 workspace
-// (zeroed by the row-term pre-pass) with TMA reduce-adds (four boxes per Q tile),
-// issued by the TMA warp; a post-pass scales and converts them.
+// (zeroed by the row-term pre-pass) with TMA reduce-adds issued by the TMA warp:
+// columns 0..63 over the tile's Q half of its stage, 64..127 over the dO half,
+// each half reduced and refilled on its own (Q first).  A post-pass scales and
+// converts them.  The LSE and D rows of a Q tile are loaded from global memory
+// before the waits they would otherwise follow.
 #include <cuda.h>
 #include <math.h>
 #include <mutex>

@@ -15,11 +15,14 @@
 // are fully masked for both Q tiles.  The (m, l, O) state carries across ring
 // steps, which is the online log-sum-exp merge of the per-step partial results.
 //
-// Warp roles (320 threads):
+// Warp roles (384 threads, three warpgroups; setmaxnreg gives the two softmax
+// warpgroups 200 registers and the third 104):
 //   warps 0-3  softmax for Q tile A (thread = row; TMEM lanes 0..127)
 //   warps 4-7  softmax for Q tile B
 //   warp  8    TMA producer: Q once, then K and V tiles into 2-stage rings
-//   warp  9    TMEM allocation and MMA issue (one thread)
+//   warp  9    TMEM allocation and MMA issue (one thread); warps 10-11 idle
+// On unmasked, unbiased tiles a row's 128 scores are read from TMEM once and both
+// softmax passes run from registers.
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512),
 // all fp32 with row i in lane i.  The softmax writes P (bf16 pairs) over the
 // first 64 columns of its S tile, and the PV product reads it from there.
