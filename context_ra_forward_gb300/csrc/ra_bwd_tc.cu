@@ -548,35 +548,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        mbar_wait(bar(kBarDSFree), (i & 1) ^ 1, P.status, kKernBwdTc, kSiteBwd));
       if (!ok) break;
       tc::fence_after_sync();
-      uint32_t dsk[32];  // dS^T as bf16 pairs, for the dK product from TMEM
 #pragma unroll
       for (int ci = 0; ci < 2; ++ci) {
         uint32_t r[32];
         tc::tmem_ld32(t_row + kColDP + 64 * h + 32 * ci, r);
         tc::tmem_wait_ld();
         const float4* dvv = dva + 8 * ci;
+        uint32_t dsk[16];  // dS^T of these 32 columns as bf16 pairs
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int u = 2 * e;
+          const float d0[4] = {dvv[u >> 2].x, dvv[u >> 2].y, dvv[u >> 2].z, dvv[u >> 2].w};
+          // P o (dP - D) for the column pair, in packed fp32 pairs
+          const float2 diff = tc::fma2(make_float2(d0[u & 3], d0[(u + 1) & 3]), make_float2(-1.f, -1.f),
+                                       make_float2(__uint_as_float(r[u]), __uint_as_float(r[u + 1])));
+          const float2 ab = tc::mul2(make_float2(p[32 * ci + u], p[32 * ci + u + 1]), diff);
+          dsk[e] = tc::pack_bf16(ab.x, ab.y);
+        }
+        // into TMEM first (the A operand of dK; over dP^T columns this warp has read:
+        // query columns 64h + 32ci.. -> TMEM columns kColDP + 64h + 16ci ..), then
+        // the 128-byte-swizzled shared-memory copy while that store completes
+        tc::tmem_st16(t_row + kColDP + 64 * h + 16 * ci, dsk);
 #pragma unroll
         for (int c8 = 0; c8 < 4; ++c8) {  // four 16-byte chunks of 8 columns
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int u = 8 * c8 + 2 * e;
-            const float d0[4] = {dvv[u >> 2].x, dvv[u >> 2].y, dvv[u >> 2].z, dvv[u >> 2].w};
-            // P o (dP - D) for the column pair, in packed fp32 pairs
-            const float2 diff = tc::fma2(make_float2(d0[u & 3], d0[(u + 1) & 3]), make_float2(-1.f, -1.f),
-                                         make_float2(__uint_as_float(r[u]), __uint_as_float(r[u + 1])));
-            const float2 ab = tc::mul2(make_float2(p[32 * ci + u], p[32 * ci + u + 1]), diff);
-            w[e] = tc::pack_bf16(ab.x, ab.y);
-            dsk[16 * ci + 4 * c8 + e] = w[e];
-          }
           const int chunk = 4 * ci + c8;  // 16-byte chunk within the 128-byte row
           const uint32_t off = (uint32_t)krow * 128u + ((uint32_t)(chunk ^ (krow & 7)) << 4);
-          *reinterpret_cast<uint4*>(ds_tile + off) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(ds_tile + off) =
+              make_uint4(dsk[4 * c8], dsk[4 * c8 + 1], dsk[4 * c8 + 2], dsk[4 * c8 + 3]);
         }
       }
-      // dS^T pairs over this warp's dP^T columns (all read above): query columns
-      // 64h..64h+63 -> TMEM columns kColDP + 64h .. + 31.
-      tc::tmem_st32(t_row + kColDP + 64 * h, dsk);
       tc::tmem_wait_st();
       fence_async_smem();
       tc::fence_before_sync();
