@@ -40,3 +40,15 @@ def test_backward_parity(case):
     compare(out["dq"], dq, dt, "dQ")
     compare(out["dk"], dk, dt, "dK")
     compare(out["dv"], dv, dt, "dV")
+
+
+def test_backward_empty_problem():
+    """S = 0: nothing to compute, nothing launched, empty gradients returned."""
+    import torch
+    import context_ra_forward_gb300 as ra
+    q = torch.empty((1, 2, 0, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((1, 2, 0), dtype=torch.float32, device="cuda")
+    before = ra.kernel_launch_count()
+    dq, dk, dv = ra.backward(q, q, q, q, lse, q, causal=True, N=4, layout="zigzag")
+    assert ra.kernel_launch_count() == before
+    assert dq.shape == dk.shape == dv.shape == q.shape
