@@ -44,6 +44,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-side-configs", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline time budget")
+    ap.add_argument("--ref-seconds", type=float, default=150.0,
+                    help="reference arm: oracle time budget over all warm-up and timed steps")
     ap.add_argument("--heads", type=int, default=None, help="override H (smaller case of the workload)")
     ap.add_argument("--seq", type=int, default=None, help="override S (smaller case of the workload)")
     return ap.parse_args()
@@ -106,10 +108,10 @@ def source_hash(files):
     return h.hexdigest()[:16]
 
 
-def committed_traffic(kernel):
+def committed_traffic(kernel, workload):
     """DRAM bytes per launch from the committed ncu summary (profiles/traffic.txt:
-    `kernel bytes source_hash source,...`), if it was taken on the kernel source as
-    it is now (else None)."""
+    `kernel workload bytes source_hash source,...`), if it was taken on this
+    workload and on the kernel source as it is now (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     try:
         with open(path) as f:
@@ -117,14 +119,14 @@ def committed_traffic(kernel):
     except OSError:
         return None
     for parts in lines:
-        if len(parts) == 4 and parts[0] == kernel:
-            sources = parts[3].split(",")
+        if len(parts) == 5 and parts[0] == kernel and parts[1] == workload:
+            sources = parts[4].split(",")
             try:
-                if source_hash(sources) != parts[2]:
+                if source_hash(sources) != parts[3]:
                     return None
             except OSError:
                 return None
-            return {"dram_bytes_per_launch": int(parts[1])}
+            return {"dram_bytes_per_launch": int(parts[2])}
     return None
 
 
@@ -230,7 +232,7 @@ def run_reference(args, w):
     _, rank, _ = rank_env()
     if rank != 0:
         return
-    per_step = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    per_step = max(2.0, min(20.0, args.ref_seconds / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         oracle_sample(w, per_step)
     vals = []
@@ -535,7 +537,7 @@ def run_ours(args, w):
         achieved = dom_fl / (phase[dom] * 1e-3) / 1e12
         peak = peaks.get("bf16_tflops_sustained") or peaks.get("bf16_tflops")
         kname = "fwd_tc_kernel" if dom == "forward" else "bwd_tc_kernel"
-        traffic = committed_traffic(kname)
+        traffic = committed_traffic(kname, w.name)
         roof = {"bound": "tensor", "kernel": kname, "achieved": round(achieved, 1), "peak": peak,
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                 "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
