@@ -22,21 +22,24 @@
 //              it also issues the bulk reduce-adds of each Q tile's dQ partial
 //   warp  9    TMEM allocation and MMA issue (one thread); warps 10-11 idle
 // TMEM (512 columns): S^T [0,128), dP^T [128,256), dK [256,384), dV [384,512);
-// all fp32 with K/V row r in lane r.  P^T (bf16 pairs) is written back over S^T
-// (Q columns 0..63 -> TMEM columns 0..31, 64..127 -> 64..95), the dQ partial of
-// a Q tile (row = query) goes into the dP^T region once that has been read.
-// dS^T (bf16) is written back over dP^T in TMEM (same column map as P^T), the A
-// operand of dK += dS^T Q, and to shared memory in the 128-byte-swizzled layout,
-// the MN-major A operand of dQ = dS K.
+// all fp32 with K/V row r in lane r.  Each softmax warp writes P^T (bf16 pairs)
+// over the first half of its 64 S^T columns (Q columns 0..63 -> TMEM columns
+// 0..31, 64..127 -> 64..95) and dS^T over the second half (-> 32..63, 96..127):
+// the A operands of dV += P^T dO and dK += dS^T Q.  dS^T also goes to shared
+// memory in the 128-byte-swizzled layout, the MN-major A operand of dQ = dS K,
+// whose result (row = query) takes the dP^T region once the dS pass has read it.
 //
-// MMA order per Q tile i:  [P^T_i] dV_i  [dS^T_i] dK_i, dQ_i -> S^T_{i+1}
-//                          [dQ_i drained] dP^T_{i+1}.
+// MMA order per Q tile i:  [P^T_i] dV_i  [dS^T_i] dQ_i, dK_i -> S^T_{i+1}
+//                          [dQ_i drained] dP^T_{i+1}
+// (the pipe runs in order, so S^T_{i+1} follows the reads of P^T_i and dS^T_i).
 // dQ partials are staged in shared memory and added into an fp32 workspace
 // (zeroed by the row-term pre-pass) with TMA reduce-adds issued by the TMA warp:
-// columns 0..63 over the tile's Q half of its stage, 64..127 over the dO half,
-// each half reduced and refilled on its own (Q first).  A post-pass scales and
-// converts them.  The LSE and D rows of a Q tile are loaded from global memory
-// before the waits they would otherwise follow.
+// columns 0..63 over the dS^T tile (which dQ_i has read), 64..127 over the dO
+// half of the tile's stage (which dV_i has read), both as soon as dQ_i is
+// complete.  The next tile's dS pass waits for the first reduce to have read the
+// dS^T tile; the Q half is refilled once dK_i has read it.  A post-pass scales
+// and converts the sums.  The LSE and D rows of a Q tile are loaded from global
+// memory before the waits they would otherwise follow.
 #include <cuda.h>
 #include <math.h>
 #include <mutex>
@@ -75,17 +78,24 @@ enum Bar {
   kBarKV = 0,
   kBarQFull = 1,    // + stage: the Q half of the stage is loaded
   kBarDOFull = 3,   // + stage: the dO half of the stage is loaded
-  // + stage: dQ columns 0..63 of a Q tile are staged over its Q half, 64..127 over
-  // its dO half.  One barrier per stage: the producer waits for tile i after it has
-  // refilled tile i-1's stage, and tile i+1 may finish before that; only tile i+2,
-  // which needs this stage refilled, could complete the next phase of the barrier.
+  // + stage: dQ columns 0..63 of tile i are staged over the dS^T tile (DrainQ),
+  // 64..127 over the dO half of its stage (DrainDO).  One barrier per stage: the
+  // producer waits for tile i after it has refilled tile i-1's stage, and tile i+1
+  // may finish before that; only tile i+2, which needs this stage refilled, could
+  // complete the next phase of the barrier.
   kBarDrainQ = 5,
   kBarDrainDO = 7,
-  kBarSFull = 9,
+  // + stage: dK_i is complete, so the Q half of tile i's stage may be refilled.
+  // Per stage for the same reason: the producer waits for it after letting the
+  // next tile's dS pass go on (kBarDPFull); only tile i+2, whose Q it has yet to
+  // load, could complete the next phase of the same barrier.
+  kBarKDone = 9,
+  kBarSFull = 11,
+  // dP^T_i is in TMEM and the reduce-add has read tile i-1's dQ columns staged over
+  // the dS^T tile (count 2: the MMA commit and the producer's arrive)
   kBarDPFull,
   kBarPReady,
   kBarDSReady,
-  kBarDSFree,
   kBarDQFull,
   kBarDQEmpty,
   kBarFinal,
@@ -293,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t cnt = 1;
       if (i == kBarPReady || i == kBarDSReady || i == kBarDQEmpty || i == kBarEpiDone) cnt = 8;
+      if (i == kBarDPFull) cnt = 2;
       if (i == kBarDrainQ || i == kBarDrainQ + 1 || i == kBarDrainDO || i == kBarDrainDO + 1) cnt = 4;
       mbar_init(bar(i), cnt);
     }
@@ -324,11 +335,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tma_load_3d(sbase + kOffK + hf * kBoxBytes, &tm_k, hf * 64, (int32_t)kp0, z, bar(kBarKV));
         tc::tma_load_3d(sbase + kOffV + hf * kBoxBytes, &tm_v, hf * 64, (int32_t)kp0, z, bar(kBarKV));
       }
-      // Stage s holds Q and dO of Q tile i (s = i & 1) and, once that tile's MMAs
-      // are done, its dQ partial: columns 0..63 over the Q half, 64..127 over the
-      // dO half.  Each half is added to the accumulator with its own bulk reduce
-      // as soon as the softmax warps have staged it, and refilled as soon as the
-      // reduce has read it: Q first, which the next S^T product needs before dO.
+      // Stage s holds Q and dO of Q tile i (s = i & 1).  Once dQ_i is complete its
+      // columns 0..63 are staged over the dS^T tile and 64..127 over the dO half;
+      // each part is added to the accumulator with its own bulk reduce as soon as
+      // the softmax warps have staged it.  The stage is refilled once both
+      // reduces have read their sources and dK_i has read Q_i (Q first).
       QWalk<kStrided> walk;
       walk.init(&P, kg0, s0);
       QTile qt;
@@ -340,6 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int hf = 0; hf < 2; ++hf)
           tc::tma_load_3d(dst + hf * kBoxBytes, tm, hf * 64, (int32_t)p0, z, bar(b + st));
       };
+      mbar_arrive(bar(kBarDPFull));  // tile 0 has no predecessor
       for (int st = 0; st < 2 && walk.next(qt); ++st) {
         load_half(&tm_q, st, 0, kBarQFull, qt.p0);
         load_half(&tm_do, st, kTileBytes, kBarDOFull, qt.p0);
@@ -349,17 +361,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < loaded; ++i) {
         const int st = i & 1;
         const uint32_t src = sbase + kOffQ + st * kStageBytes;
+        // dQ columns 0..63 from the dS^T tile first (the next tile's dS pass waits
+        // for that read), then 64..127 from the dO half; Q_{i+2} once dK_i has read Q_i
         if (!mbar_wait(bar(kBarDrainQ + st), (i >> 1) & 1, P.status, kKernBwdTc, kSiteBwd)) break;
         for (int b = 0; b < 2; ++b)  // 128-row x 32-column fp32 boxes
-          tc::tma_reduce_add_3d(&tm_dq, src + b * kBoxBytes, 32 * b, (int32_t)stage_p0[st], z);
+          tc::tma_reduce_add_3d(&tm_dq, sbase + kOffDS + b * kBoxBytes, 32 * b, (int32_t)stage_p0[st], z);
         tc::bulk_commit();
-        tc::bulk_wait_read0();  // the Q half may be overwritten from here on
-        const bool next = walk.next(qt);
-        if (next) load_half(&tm_q, st, 0, kBarQFull, qt.p0);
         if (!mbar_wait(bar(kBarDrainDO + st), (i >> 1) & 1, P.status, kKernBwdTc, kSiteBwd)) break;
         for (int b = 2; b < 4; ++b)
           tc::tma_reduce_add_3d(&tm_dq, src + b * kBoxBytes, 32 * b, (int32_t)stage_p0[st], z);
         tc::bulk_commit();
+        tc::bulk_wait_read1();
+        mbar_arrive(bar(kBarDPFull));  // for tile i+1
+        const bool next = walk.next(qt);
+        if (!mbar_wait(bar(kBarKDone + st), (i >> 1) & 1, P.status, kKernBwdTc, kSiteBwd)) break;
+        if (next) load_half(&tm_q, st, 0, kBarQFull, qt.p0);
         tc::bulk_wait_read0();
         if (next) {
           load_half(&tm_do, st, kTileBytes, kBarDOFull, qt.p0);
@@ -426,23 +442,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(bar(kBarDSReady), i & 1, P.status, kKernBwdTc, kSiteBwd);
         if (!ok) break;
         tc::fence_after_sync();
+        // dQ_i = dS K (A = dS^T MN-major, B = K MN-major) into the dP^T region, which
+        // the dS pass has read
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // dK += dS^T Q   (A = dS^T from TMEM, B MN-major)
-          const uint32_t acol = kColDP + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-          tc::mma_ts(tmem + kColDK, tmem + acol, tc::smem_desc(qb + kk * 2048, kBoxBytes, 1024), kIdescKM,
-                     (i > 0 || kk > 0) ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // dQ_i = dS K   (A = dS^T MN-major, B = K MN-major)
+        for (int kk = 0; kk < 8; ++kk) {
           tc::mma_ss(tmem + kColDP, tc::smem_desc(dsb + kk * 2048, kBoxBytes, 1024),
                      tc::smem_desc(kb + kk * 2048, kBoxBytes, 1024), kIdescMM, kk > 0);
         }
-        tc::mma_commit(bar(kBarDSFree));
         tc::mma_commit(bar(kBarDQFull));
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {  // dK += dS^T Q   (A = dS^T from TMEM, B MN-major)
+          const uint32_t acol = kColS + 32 + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+          tc::mma_ts(tmem + kColDK, tmem + acol, tc::smem_desc(qb + kk * 2048, kBoxBytes, 1024), kIdescKM,
+                     (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc::mma_commit(bar(kBarKDone + st));
         more = walk.next(qt);
         if (!more) break;
         const int nst = (i + 1) & 1;
         const uint32_t nqb = sbase + kOffQ + nst * kStageBytes, ndob = nqb + kTileBytes;
+        // S^T_{i+1} over P^T_i and dS^T_i, which dV_i and dK_i (issued before it) read
         ok = mbar_wait(bar(kBarQFull + nst), ((i + 1) >> 1) & 1, P.status, kKernBwdTc, kSiteQFull);
         if (!ok) break;
         tc::fence_after_sync();
@@ -453,6 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      kIdescKK, kk > 0);
         }
         tc::mma_commit(bar(kBarSFull));
+        // dP^T_{i+1} over dQ_i once the softmax warps have read it
         ok = mbar_wait(bar(kBarDQEmpty), i & 1, P.status, kKernBwdTc, kSiteODone) &&
              mbar_wait(bar(kBarDOFull + nst), ((i + 1) >> 1) & 1, P.status, kKernBwdTc, kSiteQFull);
         if (!ok) break;
@@ -543,9 +563,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarPReady));
 
-      // dS^T = P^T o (dP^T - D) into shared memory (bf16, 128-byte swizzle).
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarDPFull), i & 1, P.status, kKernBwdTc, kSiteSFull) &&
-                                       mbar_wait(bar(kBarDSFree), (i & 1) ^ 1, P.status, kKernBwdTc, kSiteBwd));
+      // dS^T = P^T o (dP^T - D) into TMEM and shared memory (bf16, 128-byte
+      // swizzle), once dP^T_i is complete and the reduce-add has read the previous
+      // tile's dQ columns from the dS^T tile.
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarDPFull), i & 1, P.status, kKernBwdTc, kSiteSFull));
       if (!ok) break;
       tc::fence_after_sync();
 #pragma unroll
@@ -565,10 +586,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 ab = tc::mul2(make_float2(p[32 * ci + u], p[32 * ci + u + 1]), diff);
           dsk[e] = tc::pack_bf16(ab.x, ab.y);
         }
-        // into TMEM first (the A operand of dK; over dP^T columns this warp has read:
-        // query columns 64h + 32ci.. -> TMEM columns kColDP + 64h + 16ci ..), then
-        // the 128-byte-swizzled shared-memory copy while that store completes
-        tc::tmem_st16(t_row + kColDP + 64 * h + 16 * ci, dsk);
+        // into TMEM first (the A operand of dK, in the half of this warp's S^T columns
+        // that P^T left free: query columns 64h + 32ci.. -> TMEM columns
+        // kColS + 64h + 32 + 16ci ..), then the 128-byte-swizzled shared-memory copy
+        // while that store completes
+        tc::tmem_st16(t_row + kColS + 64 * h + 32 + 16 * ci, dsk);
 #pragma unroll
         for (int c8 = 0; c8 < 4; ++c8) {  // four 16-byte chunks of 8 columns
           const int chunk = 4 * ci + c8;  // 16-byte chunk within the 128-byte row
@@ -584,8 +606,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar(kBarDSReady));
 
       // Drain this Q tile's dQ partial (TMEM lane = query row): into registers, free
-      // the TMEM region, then stage it in the tile's Q/dO stage, which the tile's
-      // finished MMAs no longer need, for the TMA warp's reduce-add.
+      // the TMEM region, then stage it in shared memory that the tile's finished
+      // MMAs no longer read, for the TMA warp's reduce-add.
       ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarDQFull), i & 1, P.status, kKernBwdTc, kSiteODone));
       if (!ok) break;
       tc::fence_after_sync();
@@ -598,9 +620,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarDQEmpty));
-        // fp32 boxes of 128 rows x 32 columns (128-byte rows, 128-byte swizzle):
-        // this warp's columns 64h..64h+63 are boxes 2h and 2h+1.
-        uint8_t* box0 = sgen + kOffQ + (i & 1) * kStageBytes + (2 * h) * kBoxBytes + krow * 128;
+        // fp32 boxes of 128 rows x 32 columns (128-byte rows, 128-byte swizzle), two
+        // per warp: columns 0..63 over the dS^T tile (free since dQ_i has read it),
+        // 64..127 over the dO half of the tile's stage (dV_i, before dQ_i, read it)
+        uint8_t* box0 = (h == 0 ? sgen + kOffDS : sgen + kOffQ + (i & 1) * kStageBytes + kTileBytes) + krow * 128;
         uint8_t* box1 = box0 + kBoxBytes;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
