@@ -21,8 +21,9 @@
 //   warps 4-7  softmax for Q tile B
 //   warp  8    TMA producer: Q once, then K and V tiles into 2-stage rings
 //   warp  9    TMEM allocation and MMA issue (one thread); warps 10-11 idle
-// On unmasked, unbiased tiles a row's 128 scores are read from TMEM once and both
-// softmax passes run from registers.
+// On unbiased tiles that are unmasked, or whose visible keys are a prefix of the
+// columns (a causal diagonal, a ragged tile), a row's 128 scores are read from
+// TMEM once and both softmax passes run from registers.
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512),
 // all fp32 with row i in lane i.  The softmax writes P (bf16 pairs) over the
 // first 64 columns of its S tile, and the PV product reads it from there.
@@ -226,11 +227,14 @@ struct RowCtx {
   const volatile int32_t* gtab;
 };
 
-enum TileKind { kPlain = 0, kLinear = 1, kGeneral = 2 };
+enum TileKind { kPlain = 0, kLinear = 1, kGeneral = 2, kMasked = 3 };
 
 // Score of column u in the log2 domain.  kPlain keeps the raw score (scaled
 // inside the exponent); kLinear adds the ALiBi bias of a tile that lies wholly
 // on one side of every query; kGeneral masks and biases element by element.
+// kMasked (no bias; the visible keys of each row are the columns up to a row
+// limit, as on a causal diagonal or a ragged tile) takes the kPlain path with the
+// columns past the limit set to -inf.
 // `lin` is the ALiBi term of this column for kLinear (c.base + c.sl * u), else unused.
 template <int kKind>
 __device__ __forceinline__ float tile_score(int u, float raw, float lin, const RowCtx& c) {
@@ -251,6 +255,15 @@ __device__ __forceinline__ float tile_score(int u, float raw, float lin, const R
 // and both passes run from registers.  The other kinds keep the two rolled TMEM
 // passes (their per-element work would not fit beside 128 held scores).
 using SRow = uint32_t[4][32];
+
+// Columns u > lim of a row are not visible: their scores become -inf.
+__device__ __forceinline__ void mask_after(SRow& sr, int lim) {
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+    for (int u = 0; u < 32; ++u)
+      if (32 * ch + u > lim) sr[ch][u] = 0xff800000u;  // -inf
+}
 
 __device__ __forceinline__ float plain_max(const SRow& sr, float c2) {
   float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -636,8 +649,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ALiBi bias linear in the column (tile on one side of every query and its
       // positions arithmetic); kGeneral: element by element.
       const bool visible_all = tile_has_rows && tile.valid == kBM && (P.causal ? below : true);
-      const int kind = !visible_all ? kGeneral
-                                    : (!alibi ? kPlain : ((below || above) && tile.step != 0 ? kLinear : kGeneral));
+      const int kind = visible_all ? (!alibi ? kPlain : ((below || above) && tile.step != 0 ? kLinear : kGeneral))
+                                   : (!alibi && (tile.step != 0 || !P.causal) ? kMasked : kGeneral);
+      // kMasked: key u of the tile is visible to this row iff u <= lim (u < valid,
+      // and under causal gk0 + step * u <= gi)
+      int lim = -1;
+      if (kind == kMasked && row_ok) {
+        lim = tile.valid - 1;
+        if (P.causal) {
+          const int64_t dlt = gi - tile.gk0;
+          if (dlt < 0) lim = -1;
+          else if (dlt < (int64_t)lim * tile.step) lim = (int)(dlt / tile.step);
+        }
+      }
       if (kind == kGeneral && tile.step == 0) {
         // Keys of this tile come from several chunks: the warp maps the 128 slots
         // (four per lane) into its own table.
@@ -691,10 +715,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Pass 1: the row max of this tile (log2 domain); pass 2: probabilities,
       // packed to bf16 pairs and stored over S columns that have already been read
       // (P column k holds scores 2k, 2k+1).
-      if (kind == kPlain) {
+      if (kind == kPlain || kind == kMasked) {
         SRow sr;
         tc::tmem_ld128(t_s, sr);
         tc::tmem_wait_ld();
+        if (kind == kMasked) mask_after(sr, lim);
         const float mu = move_max(plain_max(sr, c2));
         l += plain_probs<kFp8>(t_s, sr, mu, c2);
       } else if (kind == kLinear) {
