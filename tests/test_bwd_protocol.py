@@ -1,0 +1,360 @@
+"""A host-side model of the tensor-core backward's synchronisation
+(`bwd_tc_kernel` in csrc/ra_bwd_tc.cu), run under random timings.
+
+The model follows the kernel's roles step by step: the TMA warp (K/V once, Q and
+dO tiles into two stages, the dQ reduce-adds), the MMA thread (an in-order
+tensor pipe: S^T, dP^T, dV, dQ, dK) and the eight softmax warps (warp w: query
+column half h = w / 4, TMEM lane quarter q = w % 4).  Mbarriers keep their
+arrival counts and phases; a wait names the phase it is meant for.  TMA loads,
+reduce-adds and MMAs are asynchronous engines with random durations; the MMA
+commits arrive when every MMA issued before them has finished.  Every read and
+write of a buffer region (TMEM columns per half and lane quarter, the shared-
+memory dS^T tile, the Q and dO halves of each stage) is recorded with its time
+interval.
+
+Checked, over many random timings and tile counts:
+  * every wait ends (no deadlock);
+  * no barrier runs two phases past the phase a waiter asks for before the
+    waiter polls it (the parity of the phase would then read as not complete, or
+    as complete for the wrong phase);
+  * no write overlaps another access of the same region;
+  * every read sees the version it needs (the dS pass reads dP^T of its own tile,
+    the reduce-add reads the staged dQ of its own tile, ...).
+Planted mistakes in the model (a barrier shared by both stages, a staging buffer
+reused too early, a missing wait) must be caught.  This checks the protocol, not
+the arithmetic; the GPU parity tests check the kernel itself."""
+import heapq
+import random
+from collections import defaultdict
+
+import pytest
+
+HALVES, QUARTERS = (0, 1), (0, 1, 2, 3)
+
+
+class Barrier:
+    def __init__(self, count):
+        self.count = count
+        self.pending = count
+        self.completed = 0
+        self.waiters = []
+
+
+class Sim:
+    def __init__(self, rng, jitter):
+        self.rng = rng
+        self.jitter = jitter
+        self.queue = []
+        self.seq = 0
+        self.bars = {}
+        self.acc = defaultdict(list)
+        self.errors = []
+        self.pipe_free = 0
+        self.reduce_free = 0
+        self.groups = []
+        self.live = set()
+
+    # -- infrastructure --------------------------------------------------------
+    def d(self, lo, hi):
+        v = self.rng.randint(lo, hi)
+        if self.rng.random() < self.jitter:  # occasional long stall of one engine or warp
+            v += self.rng.randint(2000, 30000)
+        return v
+
+    def at(self, t, fn):
+        heapq.heappush(self.queue, (t, self.seq, fn))
+        self.seq += 1
+
+    def barrier(self, name, count=1):
+        self.bars[name] = Barrier(count)
+
+    def arrive(self, name, t):
+        b = self.bars[name]
+        b.pending -= 1
+        assert b.pending >= 0
+        if b.pending == 0:
+            b.completed += 1
+            b.pending = b.count
+            keep = []
+            for k, resume in b.waiters:
+                if b.completed == k + 1:
+                    self.at(t + self.rng.randint(1, 200), resume)
+                else:
+                    keep.append((k, resume))
+            b.waiters = keep
+
+    def record(self, res, t0, t1, kind, tag, who):
+        self.acc[res].append((t0, t1, kind, tag, who))
+
+    def spawn(self, name, gen):
+        self.live.add(name)
+        self.at(0, lambda t: self.advance(name, gen, t))
+
+    def advance(self, name, gen, t):
+        """Runs one role from time t (the current time of the event loop) until its
+        next step that takes time, which resumes it through the event queue: every
+        action therefore happens in global time order."""
+        def later(dt):
+            self.at(t + dt, lambda tt: self.advance(name, gen, tt))
+
+        while True:
+            try:
+                cmd = next(gen)
+            except StopIteration:
+                self.live.discard(name)
+                return
+            op = cmd[0]
+            if op == "delay":
+                later(cmd[1])
+                return
+            if op == "wait":
+                _, bname, k = cmd
+                b = self.bars[bname]
+                if b.completed == k + 1:
+                    later(1)
+                    return
+                if b.completed > k + 1:
+                    self.errors.append(f"{name}: {bname} ran past phase {k} (completed {b.completed}) before the wait")
+                    self.live.discard(name)
+                    return
+                b.waiters.append((k, lambda tt: self.advance(name, gen, tt)))
+                return
+            if op == "arrive":
+                self.arrive(cmd[1], t)
+                later(1)
+                return
+            if op == "access":  # the warp's own loads and stores: (res list, kind, tag or expected)
+                _, items, dur = cmd
+                for res, kind, tag in items:
+                    self.record(res, t, t + dur, kind, tag, name)
+                later(dur)
+                return
+            if op == "mma":
+                _, reads, writes = cmd
+                start = max(t, self.pipe_free)
+                end = start + self.d(300, 900)
+                for res, exp in reads:
+                    self.record(res, start, end, "R", exp, name)
+                for res, tag in writes:
+                    self.record(res, start, end, "W", tag, name)
+                self.pipe_free = end
+                later(self.rng.randint(5, 80))
+                return
+            if op == "commit":
+                bname = cmd[1]
+                self.at(max(t, self.pipe_free), lambda tt, b=bname: self.arrive(b, tt))
+                later(1)
+                return
+            if op == "load":
+                _, items, bname = cmd
+                end = t + self.d(400, 4000)
+                for res, tag in items:
+                    self.record(res, t, end, "W", tag, name)
+                self.at(end, lambda tt, b=bname: self.arrive(b, tt))
+                later(1)
+                return
+            if op == "reduce":
+                _, reads = cmd
+                start = max(t, self.reduce_free)
+                end = start + self.d(800, 3000)
+                for res, exp in reads:
+                    self.record(res, start, end, "R", exp, name)
+                self.reduce_free = end
+                self.groups.append(end)
+                later(1)
+                return
+            if op == "wait_read":  # all but the n most recent reduce groups have read their sources
+                n = cmd[1]
+                older = self.groups[:-n] if n else self.groups
+                later(max([t] + older) - t + 1)
+                return
+            raise ValueError(op)
+
+    def run(self):
+        while self.queue:
+            t, _, fn = heapq.heappop(self.queue)
+            fn(t)
+        if self.live:
+            self.errors.append(f"deadlock: {sorted(self.live)} never finished")
+        for res, acc in self.acc.items():
+            writes = [a for a in acc if a[2] == "W"]
+            for w in writes:
+                for a in acc:
+                    if a is not w and a[0] < w[1] and w[0] < a[1]:
+                        self.errors.append(f"{res}: {w[4]} writes {w[3]} during {a[4]} {a[2]} {a[3]}")
+            for r in acc:
+                if r[2] != "R" or r[3] is None:
+                    continue
+                prior = [w for w in writes if w[1] <= r[0]]
+                last = max(prior, key=lambda w: w[1])[3] if prior else None
+                if last != r[3]:
+                    self.errors.append(f"{res}: {r[4]} reads {last!r}, needs {r[3]!r}")
+        return self.errors
+
+
+# -- the kernel's roles ----------------------------------------------------------
+def S_all(tag=None):
+    return [(("S", h, part, q), tag) for h in HALVES for part in ("P", "dS") for q in QUARTERS]
+
+
+def DP_all(tag=None):
+    return [(("DP", h, q), tag) for h in HALVES for q in QUARTERS]
+
+
+def DS_all(tag=None):
+    return [(("DS", h, q), tag) for h in HALVES for q in QUARTERS]
+
+
+def DO_all(st, tag=None):
+    return [(("DO", st, q), tag) for q in QUARTERS]
+
+
+def stage_bar(name, i, mut):
+    """Per-stage barriers: tile i uses stage i & 1 and that barrier's phase i >> 1."""
+    if name == "KDone" and "kdone_single" in mut:
+        return "KDone0", i
+    return f"{name}{i & 1}", i >> 1
+
+
+def producer(sim, n, mut):
+    yield ("load", [(("K",), "K"), (("V",), "V")], "KV")
+    if "dpfull_no_producer" not in mut:
+        yield ("arrive", "DPFull")  # tile 0 has no predecessor
+    loaded = 0
+    for st in range(min(2, n)):
+        yield ("load", [(("Q", st), f"Q{st}")], f"QFull{st}")
+        yield ("load", [(res, f"DO{st}") for res, _ in DO_all(st)], f"DOFull{st}")
+        loaded += 1
+    i = 0
+    while i < loaded:
+        st = i & 1
+        yield ("delay", sim.d(1, 300))
+        yield ("wait",) + stage_bar("DrainQ", i, mut)
+        if "stage_q_half" in mut:
+            yield ("reduce", [(("Q", st), f"stage{i}")])
+        else:
+            yield ("reduce", DS_all(f"stage{i}"))
+        yield ("wait",) + stage_bar("DrainDO", i, mut)
+        yield ("reduce", DO_all(st, f"stage{i}"))
+        yield ("wait_read", 1)
+        if "dpfull_no_producer" not in mut:
+            yield ("arrive", "DPFull")  # for tile i+1
+        yield ("delay", sim.d(1, 100))  # the walk to tile i+2 (and any stall of this warp)
+        nxt = i + 2 < n
+        if "no_kdone_wait" not in mut:
+            yield ("wait",) + stage_bar("KDone", i, mut)
+        if nxt:
+            yield ("load", [(("Q", st), f"Q{i + 2}")], f"QFull{st}")
+        yield ("wait_read", 0)
+        if nxt:
+            yield ("load", [(res, f"DO{i + 2}") for res, _ in DO_all(st)], f"DOFull{st}")
+            loaded += 1
+        i += 1
+
+
+def mma(sim, n, mut):
+    yield ("wait", "KV", 0)
+    if n > 0:
+        yield ("wait", "QFull0", 0)
+        yield ("mma", [(("K",), "K"), (("Q", 0), "Q0")], S_all("S0"))
+        yield ("commit", "SFull")
+        yield ("wait", "DOFull0", 0)
+        yield ("mma", [(("V",), "V")] + DO_all(0, "DO0"), DP_all("dP0"))
+        yield ("commit", "DPFull")
+    for i in range(n):
+        st = i & 1
+        yield ("delay", sim.d(1, 200))
+        yield ("wait", "PReady", i)
+        yield ("mma", [(r, f"P{i}") for r, _ in S_all() if r[2] == "P"] + DO_all(st, f"DO{i}"), [])  # dV
+        yield ("wait", "DSReady", i)
+        yield ("mma", DS_all(f"dSs{i}") + [(("K",), "K")], DP_all(f"dQ{i}"))  # dQ_i over dP^T
+        yield ("commit", "DQFull")
+        yield ("mma", [(r, f"dS{i}") for r, _ in S_all() if r[2] == "dS"] + [(("Q", st), f"Q{i}")], [])  # dK
+        yield ("commit", stage_bar("KDone", i, mut)[0])
+        if i + 1 == n:
+            break
+        nst = (i + 1) & 1
+        yield ("wait", f"QFull{nst}", (i + 1) >> 1)
+        yield ("mma", [(("K",), "K"), (("Q", nst), f"Q{i + 1}")], S_all(f"S{i + 1}"))
+        yield ("commit", "SFull")
+        if "no_dqempty_wait" not in mut:
+            yield ("wait", "DQEmpty", i)
+        yield ("wait", f"DOFull{nst}", (i + 1) >> 1)
+        yield ("mma", [(("V",), "V")] + DO_all(nst, f"DO{i + 1}"), DP_all(f"dP{i + 1}"))
+        yield ("commit", "DPFull")
+    yield ("commit", "Final")
+    yield ("wait", "Final", 0)
+    yield ("wait", "EpiDone", 0)
+
+
+def softmax(sim, n, h, q, mut):
+    for i in range(n):
+        st = i & 1
+        yield ("delay", sim.d(1, 300))
+        yield ("wait", "SFull", i)
+        yield ("access", [(("S", h, "P", q), "R", f"S{i}"), (("S", h, "dS", q), "R", f"S{i}")], sim.d(200, 700))
+        yield ("delay", sim.d(300, 1200))  # probabilities
+        yield ("access", [(("S", h, "P", q), "W", f"P{i}")], sim.d(50, 300))
+        yield ("arrive", "PReady")
+        yield ("wait", "DPFull", i)
+        yield ("access", [(("DP", h, q), "R", f"dP{i}")], sim.d(100, 400))
+        yield ("delay", sim.d(100, 600))
+        yield ("access", [(("S", h, "dS", q), "W", f"dS{i}"), (("DS", h, q), "W", f"dSs{i}")], sim.d(50, 300))
+        yield ("arrive", "DSReady")
+        yield ("wait", "DQFull", i)
+        yield ("access", [(("DP", h, q), "R", f"dQ{i}")], sim.d(100, 400))
+        yield ("arrive", "DQEmpty")
+        if h == 0:
+            if "stage_q_half" in mut:
+                yield ("access", [(("Q", st), "W", f"stage{i}")], sim.d(100, 500))
+            else:
+                yield ("access", [(("DS", hh, q), "W", f"stage{i}") for hh in HALVES], sim.d(100, 500))
+            yield ("arrive", stage_bar("DrainQ", i, mut)[0])
+        else:
+            yield ("access", [(("DO", st, q), "W", f"stage{i}")], sim.d(100, 500))
+            yield ("arrive", stage_bar("DrainDO", i, mut)[0])
+    yield ("wait", "Final", 0)
+    yield ("arrive", "EpiDone")
+
+
+def simulate(seed, n, mut=(), jitter=0.05):
+    rng = random.Random(seed)
+    sim = Sim(rng, jitter)
+    sim.barrier("KV")
+    for st in (0, 1):
+        sim.barrier(f"QFull{st}")
+        sim.barrier(f"DOFull{st}")
+        sim.barrier(f"DrainQ{st}", 4)
+        sim.barrier(f"DrainDO{st}", 4)
+        sim.barrier(f"KDone{st}")
+    sim.barrier("SFull")
+    sim.barrier("DPFull", 1 if "dpfull_no_producer" in mut else 2)
+    sim.barrier("PReady", 8)
+    sim.barrier("DSReady", 8)
+    sim.barrier("DQFull")
+    sim.barrier("DQEmpty", 8)
+    sim.barrier("Final")
+    sim.barrier("EpiDone", 8)
+    sim.spawn("producer", producer(sim, n, mut))
+    sim.spawn("mma", mma(sim, n, mut))
+    for w in range(8):
+        sim.spawn(f"softmax{w}", softmax(sim, n, w >> 2, w & 3, mut))
+    return sim.run()
+
+
+def test_protocol_holds_under_random_timing():
+    for seed in range(400):
+        n = 1 + seed % 7
+        errors = simulate(seed, n, jitter=0.02 if seed % 2 else 0.1)
+        assert not errors, f"seed {seed}, {n} tiles: {errors[:3]}"
+
+
+def test_empty_walk():
+    assert not simulate(0, 0)
+
+
+@pytest.mark.parametrize("mutation", ["kdone_single", "stage_q_half", "dpfull_no_producer", "no_dqempty_wait",
+                                      "no_kdone_wait"])
+def test_planted_protocol_mistake_is_caught(mutation):
+    caught = [s for s in range(400) if simulate(s, 2 + s % 6, (mutation,), jitter=0.1)]
+    assert caught, f"{mutation} passed every timing"
