@@ -1,0 +1,175 @@
+"""Discrete-event engine for the host-side models of the tensor-core kernels'
+synchronisation (tests/test_bwd_protocol.py, tests/test_fwd_protocol.py).
+
+A role is a Python generator that yields steps: wait on a barrier for a named
+phase, arrive, spend time, read or write buffer regions, issue an MMA to the
+in-order tensor pipe, commit (arrive once every MMA issued so far has finished),
+start a TMA load (writes its regions, then arrives on its barrier) or a bulk
+reduce-add (reads its regions), and wait for older reduce-adds to have read their
+sources.  Mbarriers keep their arrival counts and completed phases.  Every
+access is recorded with its time interval; `run` reports deadlocks, barrier
+phases overtaken before their wait, writes that overlap another access of the
+same region, and reads that do not see the version they name."""
+import heapq
+from collections import defaultdict
+
+
+class Barrier:
+    def __init__(self, count):
+        self.count = count
+        self.pending = count
+        self.completed = 0
+        self.waiters = []
+
+
+class Sim:
+    def __init__(self, rng, jitter):
+        self.rng = rng
+        self.jitter = jitter
+        self.queue = []
+        self.seq = 0
+        self.bars = {}
+        self.acc = defaultdict(list)
+        self.errors = []
+        self.pipe_free = 0
+        self.reduce_free = 0
+        self.groups = []
+        self.live = set()
+
+    # -- infrastructure --------------------------------------------------------
+    def d(self, lo, hi):
+        v = self.rng.randint(lo, hi)
+        if self.rng.random() < self.jitter:  # occasional long stall of one engine or warp
+            v += self.rng.randint(2000, 30000)
+        return v
+
+    def at(self, t, fn):
+        heapq.heappush(self.queue, (t, self.seq, fn))
+        self.seq += 1
+
+    def barrier(self, name, count=1):
+        self.bars[name] = Barrier(count)
+
+    def arrive(self, name, t):
+        b = self.bars[name]
+        b.pending -= 1
+        assert b.pending >= 0
+        if b.pending == 0:
+            b.completed += 1
+            b.pending = b.count
+            keep = []
+            for k, resume in b.waiters:
+                if b.completed == k + 1:
+                    self.at(t + self.rng.randint(1, 200), resume)
+                else:
+                    keep.append((k, resume))
+            b.waiters = keep
+
+    def record(self, res, t0, t1, kind, tag, who):
+        self.acc[res].append((t0, t1, kind, tag, who))
+
+    def spawn(self, name, gen):
+        self.live.add(name)
+        self.at(0, lambda t: self.advance(name, gen, t))
+
+    def advance(self, name, gen, t):
+        """Runs one role from time t (the current time of the event loop) until its
+        next step that takes time, which resumes it through the event queue: every
+        action therefore happens in global time order."""
+        def later(dt):
+            self.at(t + dt, lambda tt: self.advance(name, gen, tt))
+
+        while True:
+            try:
+                cmd = next(gen)
+            except StopIteration:
+                self.live.discard(name)
+                return
+            op = cmd[0]
+            if op == "delay":
+                later(cmd[1])
+                return
+            if op == "wait":
+                _, bname, k = cmd
+                b = self.bars[bname]
+                if b.completed == k + 1:
+                    later(1)
+                    return
+                if b.completed > k + 1:
+                    self.errors.append(f"{name}: {bname} ran past phase {k} (completed {b.completed}) before the wait")
+                    self.live.discard(name)
+                    return
+                b.waiters.append((k, lambda tt: self.advance(name, gen, tt)))
+                return
+            if op == "arrive":
+                self.arrive(cmd[1], t)
+                later(1)
+                return
+            if op == "access":  # the warp's own loads and stores: (res list, kind, tag or expected)
+                _, items, dur = cmd
+                for res, kind, tag in items:
+                    self.record(res, t, t + dur, kind, tag, name)
+                later(dur)
+                return
+            if op == "mma":
+                _, reads, writes = cmd
+                start = max(t, self.pipe_free)
+                end = start + self.d(300, 900)
+                for res, exp in reads:
+                    self.record(res, start, end, "R", exp, name)
+                for res, tag in writes:
+                    self.record(res, start, end, "W", tag, name)
+                self.pipe_free = end
+                later(self.rng.randint(5, 80))
+                return
+            if op == "commit":
+                bname = cmd[1]
+                self.at(max(t, self.pipe_free), lambda tt, b=bname: self.arrive(b, tt))
+                later(1)
+                return
+            if op == "load":
+                _, items, bname = cmd
+                end = t + self.d(400, 4000)
+                for res, tag in items:
+                    self.record(res, t, end, "W", tag, name)
+                self.at(end, lambda tt, b=bname: self.arrive(b, tt))
+                later(1)
+                return
+            if op == "reduce":
+                _, reads = cmd
+                start = max(t, self.reduce_free)
+                end = start + self.d(800, 3000)
+                for res, exp in reads:
+                    self.record(res, start, end, "R", exp, name)
+                self.reduce_free = end
+                self.groups.append(end)
+                later(1)
+                return
+            if op == "wait_read":  # all but the n most recent reduce groups have read their sources
+                n = cmd[1]
+                older = self.groups[:-n] if n else self.groups
+                later(max([t] + older) - t + 1)
+                return
+            raise ValueError(op)
+
+    def run(self):
+        while self.queue:
+            t, _, fn = heapq.heappop(self.queue)
+            fn(t)
+        if self.live:
+            self.errors.append(f"deadlock: {sorted(self.live)} never finished")
+        for res, acc in self.acc.items():
+            writes = [a for a in acc if a[2] == "W"]
+            for w in writes:
+                for a in acc:
+                    same_op = a[4] == w[4] and a[0] == w[0] and a[1] == w[1]  # an MMA accumulating in place
+                    if a is not w and not same_op and a[0] < w[1] and w[0] < a[1]:
+                        self.errors.append(f"{res}: {w[4]} writes {w[3]} during {a[4]} {a[2]} {a[3]}")
+            for r in acc:
+                if r[2] != "R" or r[3] is None:
+                    continue
+                prior = [w for w in writes if w[1] <= r[0]]
+                last = max(prior, key=lambda w: w[1])[3] if prior else None
+                if last != r[3]:
+                    self.errors.append(f"{res}: {r[4]} reads {last!r}, needs {r[3]!r}")
+        return self.errors
