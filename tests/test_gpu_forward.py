@@ -48,6 +48,10 @@ RAGGED = [
     ("f32_nc", "f32", False, False, 3, "contiguous", 1, 2, 300, 64),
     ("n_eq_half_s", "bf16", True, False, 64, "zigzag", 1, 1, 256, 128),  # chunk = 2 tokens
     ("batch_heads", "bf16", True, False, 2, "zigzag", 3, 5, 512, 128),
+    # tiles whose visible keys are a column prefix (no ALiBi): ragged tails, diagonals
+    ("nc_ragged", "bf16", False, False, 2, "contiguous", 1, 2, 1000, 128),  # last key tile 104 wide
+    ("ct_ragged_causal", "bf16", True, False, 4, "contiguous", 1, 2, 1000, 128),
+    ("st_ragged_causal", "bf16", True, False, 3, "strided", 1, 2, 1200, 128),
     # token-strided layout: shard r holds tokens r, r+N, ...
     ("st_aligned", "bf16", True, False, 4, "strided", 1, 2, 2048, 128),     # 512 slots per shard
     ("st_alibi", "bf16", True, True, 8, "strided", 1, 2, 4096, 128),
