@@ -105,11 +105,15 @@ def mma(sim, n, mut):
         st = i & 1
         yield ("delay", sim.d(1, 200))
         yield ("wait", "PReady", i)
-        yield ("mma", [(r, f"P{i}") for r, _ in S_all() if r[2] == "P"] + DO_all(st, f"DO{i}"), [])  # dV
+        dv_prev = [(("DV", q), f"dV{i - 1}") for q in QUARTERS] if i else []  # accumulate after tile 0
+        yield ("mma", [(r, f"P{i}") for r, _ in S_all() if r[2] == "P"] + DO_all(st, f"DO{i}") + dv_prev,
+               [(("DV", q), f"dV{i}") for q in QUARTERS])
         yield ("wait", "DSReady", i)
         yield ("mma", DS_all(f"dSs{i}") + [(("K",), "K")], DP_all(f"dQ{i}"))  # dQ_i over dP^T
         yield ("commit", "DQFull")
-        yield ("mma", [(r, f"dS{i}") for r, _ in S_all() if r[2] == "dS"] + [(("Q", st), f"Q{i}")], [])  # dK
+        dk_prev = [(("DK", q), f"dK{i - 1}") for q in QUARTERS] if i else []
+        yield ("mma", [(r, f"dS{i}") for r, _ in S_all() if r[2] == "dS"] + [(("Q", st), f"Q{i}")] + dk_prev,
+               [(("DK", q), f"dK{i}") for q in QUARTERS])
         yield ("commit", stage_bar("KDone", i, mut)[0])
         if i + 1 == n:
             break
@@ -124,7 +128,11 @@ def mma(sim, n, mut):
         yield ("commit", "DPFull")
     yield ("commit", "Final")
     yield ("wait", "Final", 0)
-    yield ("wait", "EpiDone", 0)
+    if "no_epidone_wait" not in mut:
+        yield ("wait", "EpiDone", 0)
+    # TMEM is released: any later read of it would be a use after free
+    freed = S_all() + DP_all() + [(("DK", q), None) for q in QUARTERS] + [(("DV", q), None) for q in QUARTERS]
+    yield ("access", [(r, "W", "freed") for r, _ in freed], 1)
 
 
 def softmax(sim, n, h, q, mut):
@@ -154,6 +162,8 @@ def softmax(sim, n, h, q, mut):
             yield ("access", [(("DO", st, q), "W", f"stage{i}")], sim.d(100, 500))
             yield ("arrive", stage_bar("DrainDO", i, mut)[0])
     yield ("wait", "Final", 0)
+    if n > 0:  # warps 0-3 write dK out, warps 4-7 dV (an empty walk writes zeros)
+        yield ("access", [(("DK" if h == 0 else "DV", q), "R", f"{'dK' if h == 0 else 'dV'}{n - 1}")], sim.d(100, 400))
     yield ("arrive", "EpiDone")
 
 
@@ -194,7 +204,7 @@ def test_empty_walk():
 
 
 @pytest.mark.parametrize("mutation", ["kdone_single", "stage_q_half", "dpfull_no_producer", "no_dqempty_wait",
-                                      "no_kdone_wait"])
+                                      "no_kdone_wait", "no_epidone_wait"])
 def test_planted_protocol_mistake_is_caught(mutation):
     caught = [s for s in range(400) if simulate(s, 2 + s % 6, (mutation,), jitter=0.1)]
     assert caught, f"{mutation} passed every timing"

@@ -96,7 +96,10 @@ def mma(sim, n, mut, state):
                 yield ("commit", "ODone1")
     yield ("commit", "Final")
     yield ("wait", "Final", 0)
-    yield ("wait", "EpiDone", 0)
+    if "no_epidone_wait" not in mut:
+        yield ("wait", "EpiDone", 0)
+    # TMEM is released: any later read of it would be a use after free
+    yield ("access", [(r, "W", "freed") for X in TILES for r, _ in S_parts(X) + O_all(X)], 1)
 
 
 def softmax(sim, n, X, q, mut, state):
@@ -154,7 +157,8 @@ def test_protocol_holds_under_random_timing():
         assert not errors, f"seed {seed}, {n} tiles: {errors[:3]}"
 
 
-@pytest.mark.parametrize("mutation", ["no_kempty_wait", "one_kfull", "vempty_after_pv_a", "rescale_before_sfull"])
+@pytest.mark.parametrize("mutation", ["no_kempty_wait", "one_kfull", "vempty_after_pv_a", "rescale_before_sfull",
+                                      "no_epidone_wait"])
 def test_planted_protocol_mistake_is_caught(mutation):
     caught = [s for s in range(400) if simulate(s, 2 + s % 6, (mutation,), jitter=0.1)]
     assert caught, f"{mutation} passed every timing"
