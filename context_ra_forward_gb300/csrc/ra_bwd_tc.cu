@@ -62,7 +62,8 @@ constexpr int kThreads = 384;  // 3 warpgroups: softmax x2, then producer, MMA a
 // Register split (setmaxnreg, per warpgroup): the block launches with 168 per
 // thread (65536 / 384, rounded down to 8); the third warpgroup gives back to 104
 // and the softmax warpgroups take 200: 2 x 128 x 200 + 128 x 104 = 64512 = 384 x 168.
-// (The smallest split at which neither side spills.)
+// (ptxas still reports a few tens of bytes of spill traffic here, fewer than at
+// 192/120 or 208/88.)
 constexpr uint32_t kRegsSoftmax = 200, kRegsOther = 104;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDK = 256, kColDV = 384;
