@@ -84,3 +84,24 @@ def test_gpu_arm_line_small_case():
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] > 0
     if line["clocks"] is not None:                  # nvidia-smi samples during the timed region
         assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(line["clocks"])
+
+
+def test_committed_traffic_is_keyed_by_workload_and_source(tmp_path, monkeypatch):
+    """The DRAM traffic figure is reported only for the workload it was captured
+    on, and only while the kernel sources hash as they did at capture time."""
+    sys.path.insert(0, ROOT)
+    import bench
+    (tmp_path / "profiles").mkdir()
+    src = tmp_path / "k.cu"
+    src.write_text("kernel source\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h = bench.source_hash(["k.cu"])
+    (tmp_path / "profiles" / "traffic.txt").write_text(
+        "# kernel workload bytes_per_launch source_hash sources\n"
+        f"bwd_tc_kernel C5 123456 {h} k.cu\n")
+    assert bench.committed_traffic("bwd_tc_kernel", "C5") == {"dram_bytes_per_launch": 123456}
+    assert bench.committed_traffic("bwd_tc_kernel", "C3") is None
+    assert bench.committed_traffic("fwd_tc_kernel", "C5") is None
+    src.write_text("kernel source, changed\n")
+    assert bench.committed_traffic("bwd_tc_kernel", "C5") is None
+
