@@ -320,6 +320,68 @@ __device__ __forceinline__ float plain_probs(uint32_t t_s, const SRow& sr, float
   }
 }
 
+// kLinear tiles on the same register path: the bias of column u is
+// fmaf(sl, u, fmaf(sl, 32 * chunk, base)) with u an immediate, as in tile_score.
+__device__ __forceinline__ float linear_max(const SRow& sr, float c2, float base, float sl) {
+  float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch) {
+    const float lb = fmaf(sl, (float)(32 * ch), base);
+#pragma unroll
+    for (int u = 0; u < 32; u += 2)
+      mx[(u >> 1) & 3] = tc::max3(mx[(u >> 1) & 3], fmaf(__uint_as_float(sr[ch][u]), c2, fmaf(sl, (float)u, lb)),
+                                  fmaf(__uint_as_float(sr[ch][u + 1]), c2, fmaf(sl, (float)(u + 1), lb)));
+  }
+  return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+}
+
+template <bool kFp8>
+__device__ __forceinline__ float linear_probs(uint32_t t_s, const SRow& sr, float mu, float c2, float base,
+                                              float sl) {
+  // (the reference folded into the chunk's base first: a different expression
+  // from linear_max's, so the compiler does not keep 128 biases alive across both)
+  const float bm = base - mu;
+  auto x_of = [&](int ch, int u) {
+    const float lb = fmaf(sl, (float)(32 * ch), bm);
+    return fmaf(__uint_as_float(sr[ch][u]), c2, fmaf(sl, (float)u, lb));
+  };
+  if constexpr (!kFp8) {
+    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      uint32_t pk[32];
+#pragma unroll
+      for (int ci = 0; ci < 2; ++ci)
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const float pa = tc::ex2(x_of(2 * hf + ci, 2 * u)), pb = tc::ex2(x_of(2 * hf + ci, 2 * u + 1));
+          ls[u & 3] += pa + pb;
+          pk[16 * ci + u] = tc::pack_bf16(pa, pb);
+        }
+      tc::tmem_st32(t_s + 32 * hf, pk);
+    }
+    return (ls[0] + ls[1]) + (ls[2] + ls[3]);
+  } else {
+    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      uint32_t pk[16];
+#pragma unroll
+      for (int ci = 0; ci < 2; ++ci)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int ch = 2 * hf + ci;
+          const float pv[4] = {tc::ex2(x_of(ch, 4 * u)), tc::ex2(x_of(ch, 4 * u + 1)), tc::ex2(x_of(ch, 4 * u + 2)),
+                               tc::ex2(x_of(ch, 4 * u + 3))};
+          ls[u & 3] += (pv[0] + pv[1]) + (pv[2] + pv[3]);
+          pk[8 * ci + u] = tc::pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
+        }
+      tc::tmem_st16(t_s + 16 * hf, pk);
+    }
+    return (ls[0] + ls[1]) + (ls[2] + ls[3]);
+  }
+}
+
 template <int kKind>
 __device__ __forceinline__ float tile_max(uint32_t t_s, const RowCtx& c) {
   float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -723,8 +785,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mu = move_max(plain_max(sr, c2));
         l += plain_probs<kFp8>(t_s, sr, mu, c2);
       } else if (kind == kLinear) {
-        const float mu = move_max(tile_max<kLinear>(t_s, rc));
-        l += tile_probs<kLinear, kFp8>(t_s, mu, rc);
+        SRow sr;
+        tc::tmem_ld128(t_s, sr);
+        tc::tmem_wait_ld();
+        const float mu = move_max(linear_max(sr, c2, rc.base, rc.sl));
+        l += linear_probs<kFp8>(t_s, sr, mu, c2, rc.base, rc.sl);
       } else {
         const float mu = move_max(tile_max<kGeneral>(t_s, rc));
         l += tile_probs<kGeneral, kFp8>(t_s, mu, rc);
