@@ -21,9 +21,10 @@
 //   warps 4-7  softmax for Q tile B
 //   warp  8    TMA producer: Q once, then K and V tiles into 2-stage rings
 //   warp  9    TMEM allocation and MMA issue (one thread); warps 10-11 idle
-// On unbiased tiles that are unmasked, or whose visible keys are a prefix of the
-// columns (a causal diagonal, a ragged tile), a row's 128 scores are read from
-// TMEM once and both softmax passes run from registers.
+// On tiles that are unmasked (with no bias or an ALiBi bias linear in the
+// column), or unbiased with visible keys a prefix of the columns (a causal
+// diagonal, a ragged tile), a row's 128 scores are read from TMEM once and both
+// softmax passes run from registers.
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512),
 // all fp32 with row i in lane i.  The softmax writes P (bf16 pairs) over the
 // first 64 columns of its S tile, and the PV product reads it from there.
@@ -251,9 +252,9 @@ __device__ __forceinline__ float tile_score(int u, float raw, float lin, const R
   }
 }
 
-// kPlain tiles (the common case): the row's 128 scores are read from TMEM once
-// and both passes run from registers.  The other kinds keep the two rolled TMEM
-// passes (their per-element work would not fit beside 128 held scores).
+// kPlain, kMasked and kLinear tiles: the row's 128 scores are read from TMEM once
+// and both passes run from registers.  kGeneral tiles keep the two rolled TMEM
+// passes (their per-element positions would not fit beside 128 held scores).
 using SRow = uint32_t[4][32];
 
 // Columns u > lim of a row are not visible: their scores become -inf.
@@ -709,7 +710,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool above = !P.causal && tile.gmin >= qgmax; // every key at or after every query
       // kPlain: every key visible to every row, no bias; kLinear: the same with an
       // ALiBi bias linear in the column (tile on one side of every query and its
-      // positions arithmetic); kGeneral: element by element.
+      // positions arithmetic); kMasked: no bias, visible keys a prefix of the
+      // columns; kGeneral: element by element.
       const bool visible_all = tile_has_rows && tile.valid == kBM && (P.causal ? below : true);
       const int kind = visible_all ? (!alibi ? kPlain : ((below || above) && tile.step != 0 ? kLinear : kGeneral))
                                    : (!alibi && (tile.step != 0 || !P.causal) ? kMasked : kGeneral);
