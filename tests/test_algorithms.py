@@ -170,3 +170,45 @@ def test_rope_plain_fp32_angle_is_not_enough():
         exact = mpmath.mpf(t) / mpmath.power(10000, mpmath.mpf(2 * i) / 128)
         errs.append(abs(float(mpmath.mpf(naive) - exact)))
     assert max(errs) > 2.0 ** -8
+
+
+# ---------------------------------------------------------------------------- ALiBi exponents
+def _f32(x):
+    return np.float32(x)
+
+
+def _fma32(a, b, c):
+    """fp32 fused multiply-add: the product of two fp32 numbers is exact in fp64,
+    one rounding of the sum to fp32 (the second rounding through fp64 cannot
+    matter at these magnitudes for this check)."""
+    return np.float32(np.float64(a) * np.float64(b) + np.float64(c))
+
+
+def test_alibi_exponent_precision_far_from_the_diagonal():
+    """The forward's probability exponent on an ALiBi tile far below the diagonal:
+    with the row's reference folded into the tile's bias base first, the exponent
+    is formed from small numbers and keeps fp32 precision; adding the ~1e5 bias to
+    the score first (and the reference after) loses it."""
+    rng = np.random.default_rng(6)
+    slope2 = 0.5 * LOG2E           # log2-domain slope of the steepest head
+    c2 = _f32(LOG2E / math.sqrt(128))
+    dist0 = 2 ** 18 - 256          # distance of the tile's first key from the query
+    base = _f32(-slope2 * dist0)   # bias of column 0 (keys before the query)
+    sl = _f32(slope2)              # the bias grows towards the diagonal
+    raw = rng.standard_normal(128).astype(np.float32) * 8
+    exact = np.array([np.float64(r) * np.float64(c2) + np.float64(base) + np.float64(sl) * u
+                      for u, r in enumerate(raw)])
+    mu = _f32(exact.max())         # the row's reference (any value near the max will do)
+    folded, late = [], []
+    for u, r in enumerate(raw):
+        ch, uu = divmod(u, 32)
+        bm = np.float32(np.float64(base) - np.float64(mu))
+        lb = _fma32(sl, _f32(32 * ch), bm)
+        folded.append(_fma32(r, c2, _fma32(sl, _f32(uu), lb)))
+        lb0 = _fma32(sl, _f32(32 * ch), base)
+        late.append(np.float32(np.float64(_fma32(r, c2, _fma32(sl, _f32(uu), lb0))) - np.float64(mu)))
+    ref = exact - np.float64(mu)
+    err_folded = np.max(np.abs(np.array(folded, dtype=np.float64) - ref))
+    err_late = np.max(np.abs(np.array(late, dtype=np.float64) - ref))
+    assert err_folded < 1e-4, err_folded            # relative error of 2^x below 1e-4
+    assert err_late > 10 * err_folded, (err_late, err_folded)
