@@ -105,3 +105,20 @@ def test_committed_traffic_is_keyed_by_workload_and_source(tmp_path, monkeypatch
     src.write_text("kernel source, changed\n")
     assert bench.committed_traffic("bwd_tc_kernel", "C5") is None
 
+
+
+def test_flop_counts_are_the_published_convention():
+    """Useful attention flops (FlashAttention convention, causal-adjusted): 4·S²·D
+    per head forward, half of it under causal, 2.5× that for the backward — the
+    figures each workload's TFLOP/s is computed from."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from context_ra_forward_gb300 import inputs
+    expect = {"C1": (2.684e8, 0.0), "C2": (1.759e13, 0.0), "C3": (3.518e13, 0.0), "C4": (3.518e13, 0.0),
+              "C5": (2.815e14, 7.037e14)}
+    for name, (fwd, bwd) in expect.items():
+        f, b = bench.flops_of(inputs.WORKLOADS[name])
+        assert abs(f - fwd) <= 1e-3 * fwd, name
+        assert abs(b - bwd) <= 1e-3 * max(bwd, 1.0), name
+    # the strided variants do the same work as their zig-zag twins
+    assert bench.flops_of(inputs.WORKLOADS["C5S"]) == bench.flops_of(inputs.WORKLOADS["C5"])
