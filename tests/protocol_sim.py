@@ -9,9 +9,21 @@ reduce-add (reads its regions), and wait for older reduce-adds to have read thei
 sources.  Mbarriers keep their arrival counts and completed phases.  Every
 access is recorded with its time interval; `run` reports deadlocks, barrier
 phases overtaken before their wait, writes that overlap another access of the
-same region, and reads that do not see the version they name."""
+same region, and reads that do not see the version they name.
+
+A wait returns whether its phase completed (`ok = yield ("wait", ...)`).  With a
+fault injected (`fault=(role, n)`: that role's n-th wait never completes) the
+run takes the kernels' failure path: the failed wait sets the status word, and
+from then on every wait that has lasted longer than the status-check interval
+returns False, as the kernels' bounded waits do.  Such a run is checked for what
+must hold even after a failure: every role ends, no asynchronous operation is
+still running when the last role ends, and nothing touches tensor memory after
+it is released (version checks are off: the results are flagged as failed)."""
 import heapq
 from collections import defaultdict
+
+
+STATUS_CHECK = 100_000  # a wait consults the status word after this long (~50 us)
 
 
 class Barrier:
@@ -23,9 +35,13 @@ class Barrier:
 
 
 class Sim:
-    def __init__(self, rng, jitter):
+    def __init__(self, rng, jitter, fault=None):
         self.rng = rng
         self.jitter = jitter
+        self.fault = fault
+        self.status = False
+        self.waits_done = defaultdict(int)
+        self.finish = {}
         self.queue = []
         self.seq = 0
         self.bars = {}
@@ -58,12 +74,26 @@ class Sim:
             b.completed += 1
             b.pending = b.count
             keep = []
-            for k, resume in b.waiters:
-                if b.completed == k + 1:
-                    self.at(t + self.rng.randint(1, 200), resume)
+            for w in b.waiters:
+                if b.completed == w["k"] + 1:
+                    self.wake(w, t + self.rng.randint(1, 200), True)
                 else:
-                    keep.append((k, resume))
+                    keep.append(w)
             b.waiters = keep
+
+    def wake(self, w, t, value):
+        if not w["done"]:
+            w["done"] = True
+            self.at(t, lambda tt: w["resume"](tt, value))
+
+    def set_status(self, t):
+        """A wait failed: every pending wait gives up once it has lasted STATUS_CHECK."""
+        if self.status:
+            return
+        self.status = True
+        for b in self.bars.values():
+            for w in b.waiters:
+                self.at(max(t, w["start"] + STATUS_CHECK), lambda tt, w=w: self.wake(w, tt, False))
 
     def record(self, res, t0, t1, kind, tag, who):
         self.acc[res].append((t0, t1, kind, tag, who))
@@ -72,19 +102,21 @@ class Sim:
         self.live.add(name)
         self.at(0, lambda t: self.advance(name, gen, t))
 
-    def advance(self, name, gen, t):
+    def advance(self, name, gen, t, value=None):
         """Runs one role from time t (the current time of the event loop) until its
         next step that takes time, which resumes it through the event queue: every
         action therefore happens in global time order."""
-        def later(dt):
-            self.at(t + dt, lambda tt: self.advance(name, gen, tt))
+        def later(dt, v=None):
+            self.at(t + dt, lambda tt: self.advance(name, gen, tt, v))
 
         while True:
             try:
-                cmd = next(gen)
+                cmd = gen.send(value)
             except StopIteration:
                 self.live.discard(name)
+                self.finish[name] = t
                 return
+            value = None
             op = cmd[0]
             if op == "delay":
                 later(cmd[1])
@@ -92,14 +124,23 @@ class Sim:
             if op == "wait":
                 _, bname, k = cmd
                 b = self.bars[bname]
+                self.waits_done[name] += 1
+                if self.fault == (name, self.waits_done[name]):  # this phase never completes
+                    self.set_status(t)
+                    later(STATUS_CHECK, False)
+                    return
                 if b.completed == k + 1:
-                    later(1)
+                    later(1, True)
                     return
                 if b.completed > k + 1:
                     self.errors.append(f"{name}: {bname} ran past phase {k} (completed {b.completed}) before the wait")
                     self.live.discard(name)
                     return
-                b.waiters.append((k, lambda tt: self.advance(name, gen, tt)))
+                w = {"k": k, "start": t, "done": False,
+                     "resume": lambda tt, v: self.advance(name, gen, tt, v)}
+                b.waiters.append(w)
+                if self.status:
+                    self.at(t + STATUS_CHECK, lambda tt: self.wake(w, tt, False))
                 return
             if op == "arrive":
                 self.arrive(cmd[1], t)
@@ -158,6 +199,8 @@ class Sim:
             fn(t)
         if self.live:
             self.errors.append(f"deadlock: {sorted(self.live)} never finished")
+        if self.fault is not None:
+            return self.failure_checks()
         for res, acc in self.acc.items():
             writes = [a for a in acc if a[2] == "W"]
             for w in writes:
@@ -172,4 +215,17 @@ class Sim:
                 last = max(prior, key=lambda w: w[1])[3] if prior else None
                 if last != r[3]:
                     self.errors.append(f"{res}: {r[4]} reads {last!r}, needs {r[3]!r}")
+        return self.errors
+
+    def failure_checks(self):
+        """After an injected fault: nothing still running when the last role ends,
+        nothing touching a region after its release (a write tagged "freed")."""
+        end = max(self.finish.values(), default=0)
+        for res, acc in self.acc.items():
+            freed = [a for a in acc if a[3] == "freed"]
+            for a in acc:
+                if a[1] > end:
+                    self.errors.append(f"{res}: {a[4]} {a[2]} {a[3]} still running when the last role ended")
+                if freed and a[3] != "freed" and a[1] > freed[0][0]:
+                    self.errors.append(f"{res}: {a[4]} {a[2]} {a[3]} after the release")
         return self.errors

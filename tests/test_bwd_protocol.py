@@ -21,7 +21,12 @@ Checked, over many random timings and tile counts:
   * every read sees the version it needs (the dS pass reads dP^T of its own tile,
     the reduce-add reads the staged dQ of its own tile, ...).
 Planted mistakes in the model (a barrier shared by both stages, a staging buffer
-reused too early, a missing wait) must be caught.  This checks the protocol, not
+reused too early, a missing wait) must be caught.
+
+Failure paths: with a wait that never completes injected at every wait of every
+role in turn, the roles take the kernel's error exits; every role must still
+end, no MMA, load or reduce-add may be running when the last one ends, and
+nothing may touch TMEM after its release.  This checks the protocol, not
 the arithmetic; the GPU parity tests check the kernel itself."""
 import random
 
@@ -69,12 +74,14 @@ def producer(sim, n, mut):
     while i < loaded:
         st = i & 1
         yield ("delay", sim.d(1, 300))
-        yield ("wait",) + stage_bar("DrainQ", i, mut)
+        if not (yield ("wait",) + stage_bar("DrainQ", i, mut)):
+            break
         if "stage_q_half" in mut:
             yield ("reduce", [(("Q", st), f"stage{i}")])
         else:
             yield ("reduce", DS_all(f"stage{i}"))
-        yield ("wait",) + stage_bar("DrainDO", i, mut)
+        if not (yield ("wait",) + stage_bar("DrainDO", i, mut)):
+            break
         yield ("reduce", DO_all(st, f"stage{i}"))
         yield ("wait_read", 1)
         if "dpfull_no_producer" not in mut:
@@ -82,7 +89,8 @@ def producer(sim, n, mut):
         yield ("delay", sim.d(1, 100))  # the walk to tile i+2 (and any stall of this warp)
         nxt = i + 2 < n
         if "no_kdone_wait" not in mut:
-            yield ("wait",) + stage_bar("KDone", i, mut)
+            if not (yield ("wait",) + stage_bar("KDone", i, mut)):
+                break
         if nxt:
             yield ("load", [(("Q", st), f"Q{i + 2}")], f"QFull{st}")
         yield ("wait_read", 0)
@@ -90,25 +98,38 @@ def producer(sim, n, mut):
             yield ("load", [(res, f"DO{i + 2}") for res, _ in DO_all(st)], f"DOFull{st}")
             loaded += 1
         i += 1
+    # every reduce-add complete and every load landed before the CTA may exit
+    yield ("wait_read", 0)
+    yield ("wait", "KV", 0)
+    for back in (1, 2):
+        if back <= loaded:
+            ii = loaded - back
+            yield ("wait", f"QFull{ii & 1}", ii >> 1)
+            yield ("wait", f"DOFull{ii & 1}", ii >> 1)
 
 
 def mma(sim, n, mut):
-    yield ("wait", "KV", 0)
-    if n > 0:
-        yield ("wait", "QFull0", 0)
-        yield ("mma", [(("K",), "K"), (("Q", 0), "Q0")], S_all("S0"))
-        yield ("commit", "SFull")
-        yield ("wait", "DOFull0", 0)
-        yield ("mma", [(("V",), "V")] + DO_all(0, "DO0"), DP_all("dP0"))
-        yield ("commit", "DPFull")
-    for i in range(n):
+    ok = yield ("wait", "KV", 0)
+    if ok and n > 0:
+        ok = yield ("wait", "QFull0", 0)
+        if ok:
+            yield ("mma", [(("K",), "K"), (("Q", 0), "Q0")], S_all("S0"))
+            yield ("commit", "SFull")
+            ok = yield ("wait", "DOFull0", 0)
+        if ok:
+            yield ("mma", [(("V",), "V")] + DO_all(0, "DO0"), DP_all("dP0"))
+            yield ("commit", "DPFull")
+    i = 0
+    while ok and i < n:
         st = i & 1
         yield ("delay", sim.d(1, 200))
-        yield ("wait", "PReady", i)
+        if not (yield ("wait", "PReady", i)):
+            break
         dv_prev = [(("DV", q), f"dV{i - 1}") for q in QUARTERS] if i else []  # accumulate after tile 0
         yield ("mma", [(r, f"P{i}") for r, _ in S_all() if r[2] == "P"] + DO_all(st, f"DO{i}") + dv_prev,
                [(("DV", q), f"dV{i}") for q in QUARTERS])
-        yield ("wait", "DSReady", i)
+        if not (yield ("wait", "DSReady", i)):
+            break
         yield ("mma", DS_all(f"dSs{i}") + [(("K",), "K")], DP_all(f"dQ{i}"))  # dQ_i over dP^T
         yield ("commit", "DQFull")
         dk_prev = [(("DK", q), f"dK{i - 1}") for q in QUARTERS] if i else []
@@ -118,38 +139,49 @@ def mma(sim, n, mut):
         if i + 1 == n:
             break
         nst = (i + 1) & 1
-        yield ("wait", f"QFull{nst}", (i + 1) >> 1)
+        if not (yield ("wait", f"QFull{nst}", (i + 1) >> 1)):
+            break
         yield ("mma", [(("K",), "K"), (("Q", nst), f"Q{i + 1}")], S_all(f"S{i + 1}"))
         yield ("commit", "SFull")
         if "no_dqempty_wait" not in mut:
-            yield ("wait", "DQEmpty", i)
-        yield ("wait", f"DOFull{nst}", (i + 1) >> 1)
+            if not (yield ("wait", "DQEmpty", i)):
+                break
+        if not (yield ("wait", f"DOFull{nst}", (i + 1) >> 1)):
+            break
         yield ("mma", [(("V",), "V")] + DO_all(nst, f"DO{i + 1}"), DP_all(f"dP{i + 1}"))
         yield ("commit", "DPFull")
+        i += 1
+    # every MMA issued so far complete, the epilogue's reads done, then TMEM released
     yield ("commit", "Final")
     yield ("wait", "Final", 0)
     if "no_epidone_wait" not in mut:
         yield ("wait", "EpiDone", 0)
-    # TMEM is released: any later read of it would be a use after free
     freed = S_all() + DP_all() + [(("DK", q), None) for q in QUARTERS] + [(("DV", q), None) for q in QUARTERS]
     yield ("access", [(r, "W", "freed") for r, _ in freed], 1)
 
 
 def softmax(sim, n, h, q, mut):
+    ok = True
     for i in range(n):
         st = i & 1
         yield ("delay", sim.d(1, 300))
-        yield ("wait", "SFull", i)
+        ok = yield ("wait", "SFull", i)
+        if not ok:
+            break
         yield ("access", [(("S", h, "P", q), "R", f"S{i}"), (("S", h, "dS", q), "R", f"S{i}")], sim.d(200, 700))
         yield ("delay", sim.d(300, 1200))  # probabilities
         yield ("access", [(("S", h, "P", q), "W", f"P{i}")], sim.d(50, 300))
         yield ("arrive", "PReady")
-        yield ("wait", "DPFull", i)
+        ok = yield ("wait", "DPFull", i)
+        if not ok:
+            break
         yield ("access", [(("DP", h, q), "R", f"dP{i}")], sim.d(100, 400))
         yield ("delay", sim.d(100, 600))
         yield ("access", [(("S", h, "dS", q), "W", f"dS{i}"), (("DS", h, q), "W", f"dSs{i}")], sim.d(50, 300))
         yield ("arrive", "DSReady")
-        yield ("wait", "DQFull", i)
+        ok = yield ("wait", "DQFull", i)
+        if not ok:
+            break
         yield ("access", [(("DP", h, q), "R", f"dQ{i}")], sim.d(100, 400))
         yield ("arrive", "DQEmpty")
         if h == 0:
@@ -161,15 +193,17 @@ def softmax(sim, n, h, q, mut):
         else:
             yield ("access", [(("DO", st, q), "W", f"stage{i}")], sim.d(100, 500))
             yield ("arrive", stage_bar("DrainDO", i, mut)[0])
-    yield ("wait", "Final", 0)
-    if n > 0:  # warps 0-3 write dK out, warps 4-7 dV (an empty walk writes zeros)
-        yield ("access", [(("DK" if h == 0 else "DV", q), "R", f"{'dK' if h == 0 else 'dV'}{n - 1}")], sim.d(100, 400))
+    if ok:
+        ok = yield ("wait", "Final", 0)
+    if ok:  # warps 0-3 write dK out, warps 4-7 dV (an empty walk writes zeros)
+        yield ("access", [(("DK" if h == 0 else "DV", q), "R", f"{'dK' if h == 0 else 'dV'}{n - 1}" if n else None)],
+               sim.d(100, 400))
     yield ("arrive", "EpiDone")
 
 
-def simulate(seed, n, mut=(), jitter=0.05):
+def simulate(seed, n, mut=(), jitter=0.05, fault=None, keep=False):
     rng = random.Random(seed)
-    sim = Sim(rng, jitter)
+    sim = Sim(rng, jitter, fault)
     sim.barrier("KV")
     for st in (0, 1):
         sim.barrier(f"QFull{st}")
@@ -189,7 +223,8 @@ def simulate(seed, n, mut=(), jitter=0.05):
     sim.spawn("mma", mma(sim, n, mut))
     for w in range(8):
         sim.spawn(f"softmax{w}", softmax(sim, n, w >> 2, w & 3, mut))
-    return sim.run()
+    errors = sim.run()
+    return (errors, sim) if keep else errors
 
 
 def test_protocol_holds_under_random_timing():
@@ -208,3 +243,25 @@ def test_empty_walk():
 def test_planted_protocol_mistake_is_caught(mutation):
     caught = [s for s in range(400) if simulate(s, 2 + s % 6, (mutation,), jitter=0.1)]
     assert caught, f"{mutation} passed every timing"
+
+
+def _faults(seed, n):
+    """Every wait of every role, in a clean run of the same timing."""
+    _, sim = simulate(seed, n, keep=True)
+    return [(role, k) for role, count in sorted(sim.waits_done.items()) for k in range(1, count + 1)]
+
+
+@pytest.mark.parametrize("n", [1, 2, 5])
+def test_failure_paths(n):
+    """A wait that never completes, at every wait of every role: every role still
+    ends, no MMA, load or reduce-add is running when the last one does, and
+    nothing touches TMEM after it is released."""
+    for seed in (11, 12):
+        for fault in _faults(seed, n):
+            errors = simulate(seed, n, fault=fault)
+            assert not errors, f"seed {seed}, {n} tiles, fault {fault}: {errors[:3]}"
+
+
+def test_release_without_epilogue_barrier_is_caught_after_a_fault():
+    caught = any(simulate(11, 5, ("no_epidone_wait",), fault=f) for f in _faults(11, 5))
+    assert caught
