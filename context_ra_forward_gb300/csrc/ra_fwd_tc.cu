@@ -21,10 +21,16 @@
 //   warps 4-7  softmax for Q tile B
 //   warp  8    TMA producer: Q once, then K and V tiles into 2-stage rings
 //   warp  9    TMEM allocation and MMA issue (one thread); warps 10-11 idle
-// On tiles that are unmasked (with no bias or an ALiBi bias linear in the
-// column), or unbiased with visible keys a prefix of the columns (a causal
-// diagonal, a ragged tile), a row's 128 scores are read from TMEM once and both
-// softmax passes run from registers.
+// On tiles that are unmasked, or whose visible keys are a prefix of the columns
+// (a causal diagonal, a ragged tile), a row's 128 scores are read from TMEM once
+// and both softmax passes run from registers.
+// Causal ALiBi (bf16): every visible key lies at or before its query, so the bias
+// -slope*(g_i - g_j) is linear in the key: a per-row constant plus slope*step*u
+// for column u of the tile.  The column term is added to the scores by the
+// tensor core (one more K = 16 step of the Q K^T product against a fixed block:
+// ones for Q, the column term split into four bf16 parts for K), and the row
+// constant is an offset of the row's reference; the tiles then take the register
+// path of unbiased tiles.
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512),
 // all fp32 with row i in lane i.  The softmax writes P (bf16 pairs) over the
 // first 64 columns of its S tile, and the PV product reads it from there.
@@ -97,7 +103,12 @@ struct FwdCfg {
   static constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
   static constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr uint32_t kOffGtab = kOffTmemSlot + 16;             // 8 warps x 128 int32 key positions
-  static constexpr uint32_t kSmemBytes = kOffGtab + 8 * kBM * 4 + 1024;  // + alignment slack
+  // ALiBi column-term blocks (bf16 only), 128-byte swizzled like the tiles, of
+  // which the MMA reads the first 32 bytes (K = 16) of every row: one 8-row atom
+  // of ones for Q (read with an 8-row-group stride of 0), 128 rows for K.
+  static constexpr uint32_t kOffQext = (kOffGtab + 8 * kBM * 4 + 1023u) & ~1023u;
+  static constexpr uint32_t kOffKext = kOffQext + 1024;
+  static constexpr uint32_t kSmemBytes = kOffKext + kBM * 128 + 1024;  // + alignment slack
   // Q (K-major) x K (K-major); P (TMEM) x V (MN-major)
   static constexpr uint32_t kIdescS = kFp8 ? tc::idesc_e4m3(128, 128, 0, 0) : tc::idesc_bf16(128, 128, 0, 0);
   static constexpr uint32_t kIdescPV = kFp8 ? tc::idesc_e4m3(128, 128, 0, 1) : tc::idesc_bf16(128, 128, 0, 1);
@@ -111,6 +122,7 @@ struct FwdParams {
   int32_t causal;
   int32_t aligned;      // every 256-row query pair and 128-row tile lies in one run
   int32_t heavy_first;  // causal + aligned: CTAs ordered by decreasing work
+  int32_t alibi_mma;    // causal + aligned + ALiBi + bf16: the column term rides on the Q K^T product
   const float* slopes;
   float c2;             // softmax scale * log2(e) (for e4m3: times the Q and K scales)
   float o_scale;        // V scale (1 for bf16)
@@ -252,9 +264,10 @@ __device__ __forceinline__ float tile_score(int u, float raw, float lin, const R
   }
 }
 
-// kPlain, kMasked and kLinear tiles: the row's 128 scores are read from TMEM once
-// and both passes run from registers.  kGeneral tiles keep the two rolled TMEM
-// passes (their per-element positions would not fit beside 128 held scores).
+// kPlain and kMasked tiles: the row's 128 scores are read from TMEM once and both
+// passes run from registers.  kLinear and kGeneral tiles keep the two rolled TMEM
+// passes (their per-column bias terms or per-element positions would not fit
+// beside 128 held scores without spilling).
 using SRow = uint32_t[4][32];
 
 // Columns u > lim of a row are not visible: their scores become -inf.
@@ -321,68 +334,6 @@ __device__ __forceinline__ float plain_probs(uint32_t t_s, const SRow& sr, float
   }
 }
 
-// kLinear tiles on the same register path: the bias of column u is
-// fmaf(sl, u, fmaf(sl, 32 * chunk, base)) with u an immediate, as in tile_score.
-__device__ __forceinline__ float linear_max(const SRow& sr, float c2, float base, float sl) {
-  float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-  for (int ch = 0; ch < 4; ++ch) {
-    const float lb = fmaf(sl, (float)(32 * ch), base);
-#pragma unroll
-    for (int u = 0; u < 32; u += 2)
-      mx[(u >> 1) & 3] = tc::max3(mx[(u >> 1) & 3], fmaf(__uint_as_float(sr[ch][u]), c2, fmaf(sl, (float)u, lb)),
-                                  fmaf(__uint_as_float(sr[ch][u + 1]), c2, fmaf(sl, (float)(u + 1), lb)));
-  }
-  return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-}
-
-template <bool kFp8>
-__device__ __forceinline__ float linear_probs(uint32_t t_s, const SRow& sr, float mu, float c2, float base,
-                                              float sl) {
-  // (the reference folded into the chunk's base first: a different expression
-  // from linear_max's, so the compiler does not keep 128 biases alive across both)
-  const float bm = base - mu;
-  auto x_of = [&](int ch, int u) {
-    const float lb = fmaf(sl, (float)(32 * ch), bm);
-    return fmaf(__uint_as_float(sr[ch][u]), c2, fmaf(sl, (float)u, lb));
-  };
-  if constexpr (!kFp8) {
-    float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      uint32_t pk[32];
-#pragma unroll
-      for (int ci = 0; ci < 2; ++ci)
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const float pa = tc::ex2(x_of(2 * hf + ci, 2 * u)), pb = tc::ex2(x_of(2 * hf + ci, 2 * u + 1));
-          ls[u & 3] += pa + pb;
-          pk[16 * ci + u] = tc::pack_bf16(pa, pb);
-        }
-      tc::tmem_st32(t_s + 32 * hf, pk);
-    }
-    return (ls[0] + ls[1]) + (ls[2] + ls[3]);
-  } else {
-    float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      uint32_t pk[16];
-#pragma unroll
-      for (int ci = 0; ci < 2; ++ci)
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int ch = 2 * hf + ci;
-          const float pv[4] = {tc::ex2(x_of(ch, 4 * u)), tc::ex2(x_of(ch, 4 * u + 1)), tc::ex2(x_of(ch, 4 * u + 2)),
-                               tc::ex2(x_of(ch, 4 * u + 3))};
-          ls[u & 3] += (pv[0] + pv[1]) + (pv[2] + pv[3]);
-          pk[8 * ci + u] = tc::pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
-        }
-      tc::tmem_st16(t_s + 16 * hf, pk);
-    }
-    return (ls[0] + ls[1]) + (ls[2] + ls[3]);
-  }
-}
-
 template <int kKind>
 __device__ __forceinline__ float tile_max(uint32_t t_s, const RowCtx& c) {
   float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -416,7 +367,9 @@ __device__ __forceinline__ float tile_probs(uint32_t t_s, float mu, const RowCtx
 #pragma unroll 1
     for (int hf = 0; hf < 2; ++hf) {
       uint32_t pk[32];
-      const float lb = fmaf(c.sl, (float)(64 * hf), c.base);
+      // kLinear: the row's reference folded into the bias base first, so the
+      // exponent is formed from small numbers even where the bias is large
+      const float lbm = fmaf(c.sl, (float)(64 * hf), c.base - mu);
 #pragma unroll
       for (int ci = 0; ci < 2; ++ci) {
         uint32_t r[32];
@@ -433,7 +386,7 @@ __device__ __forceinline__ float tile_probs(uint32_t t_s, float mu, const RowCtx
             // raw * c2 + (ALiBi term of the column - mu)
             const float2 lin = tc::fma2(make_float2(c.sl, c.sl),
                                         make_float2((float)(32 * ci + 2 * u), (float)(32 * ci + 2 * u + 1)),
-                                        make_float2(lb - mu, lb - mu));
+                                        make_float2(lbm, lbm));
             x = tc::fma2(make_float2(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1])),
                          make_float2(c.c2, c.c2), lin);
           } else {
@@ -453,7 +406,7 @@ __device__ __forceinline__ float tile_probs(uint32_t t_s, float mu, const RowCtx
 #pragma unroll 1
     for (int hf = 0; hf < 2; ++hf) {
       uint32_t pk[16];
-      const float lb = fmaf(c.sl, (float)(64 * hf), c.base);
+      const float lbm = fmaf(c.sl, (float)(64 * hf), c.base - mu);  // kLinear, as above
 #pragma unroll
       for (int ci = 0; ci < 2; ++ci) {
         uint32_t r[32];
@@ -465,7 +418,9 @@ __device__ __forceinline__ float tile_probs(uint32_t t_s, float mu, const RowCtx
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int cc = 32 * ci + 4 * u + e;
-            pv[e] = prob(tile_score<kKind>(64 * hf + cc, __uint_as_float(r[4 * u + e]), fmaf(c.sl, (float)cc, lb), c));
+            const float raw = __uint_as_float(r[4 * u + e]);
+            if constexpr (kKind == kLinear) pv[e] = tc::ex2(fmaf(raw, c.c2, fmaf(c.sl, (float)cc, lbm)));
+            else pv[e] = prob(tile_score<kKind>(64 * hf + cc, raw, 0.f, c));
           }
           ls[u & 3] += (pv[0] + pv[1]) + (pv[2] + pv[3]);
           pk[8 * ci + u] = tc::pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
@@ -478,8 +433,65 @@ __device__ __forceinline__ float tile_probs(uint32_t t_s, float mu, const RowCtx
   return (ls[0] + ls[1]) + (ls[2] + ls[3]);
 }
 
+// The column term is taken relative to the tile's middle column (kBiasMid), which
+// halves its largest magnitude, slope2 * step * 64 in log2 units.  The fp32 score
+// accumulator holds the term to about 2^-24 of that; up to kMaxMmaColumnTerm
+// (≈ 1.2e-4 in the exponent, far below the bf16 rounding of P) the tensor core
+// carries it, and steeper slopes keep the per-element path.
+constexpr int kBiasMid = 64;
+constexpr float kMaxMmaColumnTerm = 2048.0f;
+
+// Whether this CTA's head carries its ALiBi column term on the Q K^T product
+// (every role evaluates the same expression on the same inputs).
+__device__ __forceinline__ bool bias_on_mma(const FwdParams& P, int hh) {
+  if (!P.alibi_mma) return false;
+  const float t = fabsf(P.slopes[hh] * kLog2e) * (float)P.map.run_step() * (float)kBiasMid;
+  return t <= kMaxMmaColumnTerm;  // false for NaN slopes too
+}
+
+// Fills the column-term blocks: K row u holds the four bf16 parts of
+// w_u = slope2 * step * (u - 64) / c2 (the term in raw-score units, so that
+// c2 * w_u is the log2-domain bias of column u relative to column 64) in columns
+// 0..3 and zeros in 4..15; every Q row holds ones in columns 0..3.  Row r of an
+// 8-row atom keeps its 16-byte chunk c at chunk c ^ r (the 128-byte swizzle).
+// Called by threads 0..135 before the block-wide barrier that precedes the first MMA.
+__device__ __forceinline__ void fill_bias_blocks(uint8_t* qext, uint8_t* kext, float slope2, float step,
+                                                 float c2) {
+  const int t = threadIdx.x;
+  uint32_t w[4] = {0u, 0u, 0u, 0u};  // chunk 0 of the row: 8 bf16 as 4 pairs
+  uint8_t* row;
+  int r;
+  if (t < kBM) {
+    // the exact term in fp64, then four successive bf16 roundings of what is left
+    double rest = (double)slope2 * (double)step * (double)(t - kBiasMid) / (double)c2;
+    __nv_bfloat16 part[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      part[i] = __double2bfloat16(rest);
+      rest -= (double)__bfloat162float(part[i]);
+    }
+    w[0] = (uint32_t)__bfloat16_as_ushort(part[0]) | ((uint32_t)__bfloat16_as_ushort(part[1]) << 16);
+    w[1] = (uint32_t)__bfloat16_as_ushort(part[2]) | ((uint32_t)__bfloat16_as_ushort(part[3]) << 16);
+    row = kext + (t >> 3) * 1024;
+    r = t & 7;
+  } else if (t < kBM + 8) {
+    const uint32_t one = (uint32_t)__bfloat16_as_ushort(__float2bfloat16(1.0f));
+    w[0] = w[1] = one | (one << 16);
+    row = qext;
+    r = t - kBM;
+  } else {
+    return;
+  }
+  uint4* chunk0 = reinterpret_cast<uint4*>(row + r * 128 + ((0 ^ r) << 4));
+  uint4* chunk1 = reinterpret_cast<uint4*>(row + r * 128 + ((1 ^ r) << 4));
+  *chunk0 = make_uint4(w[0], w[1], w[2], w[3]);
+  *chunk1 = make_uint4(0u, 0u, 0u, 0u);
+  // make the generic-proxy stores visible to the tensor core's reads
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 template <bool kFp8>
-__device__ __forceinline__ void issue_s(uint32_t tmem, uint32_t sbase, int X, int ks) {
+__device__ __forceinline__ void issue_s(uint32_t tmem, uint32_t sbase, int X, int ks, bool bias_mma) {
   using C = FwdCfg<kFp8>;
   const uint32_t qa = sbase + C::kOffQ + X * C::kTileBytes;
   const uint32_t kb = sbase + C::kOffK + ks * C::kTileBytes;
@@ -491,6 +503,14 @@ __device__ __forceinline__ void issue_s(uint32_t tmem, uint32_t sbase, int X, in
     const uint64_t b = tc::smem_desc(kb + off, 16, 1024);
     if constexpr (kFp8) tc::mma_ss_f8(tmem + X * 128, a, b, C::kIdescS, kk > 0 ? 1u : 0u);
     else tc::mma_ss(tmem + X * 128, a, b, C::kIdescS, kk > 0 ? 1u : 0u);
+  }
+  if constexpr (!kFp8) {
+    if (bias_mma) {
+      // + ones . (column term): the 8-row Q atom serves all 16 row groups (stride 0)
+      const uint64_t a = tc::smem_desc(sbase + C::kOffQext, 16, 0);
+      const uint64_t b = tc::smem_desc(sbase + C::kOffKext, 16, 1024);
+      tc::mma_ss(tmem + X * 128, a, b, C::kIdescS, 1u);
+    }
   }
 }
 
@@ -510,7 +530,13 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t sbase, int X, i
   }
 }
 
-template <bool kFp8>
+// How a kernel instantiation adds the ALiBi bias: not at all (no slopes), on the
+// tensor core (causal, aligned, bf16: see the header), or per element in the
+// softmax (every other case).  Each instantiation holds only the tile paths its
+// case uses, which keeps the softmax warps' registers within their budget.
+enum BiasMode { kBiasNone = 0, kBiasMma = 1, kBiasElem = 2 };
+
+template <bool kFp8, int kBias>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ FwdParams P) {
@@ -541,6 +567,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   int64_t pair_gmin, pair_gmax;
   m.grange(P0, qend, pair_gmin, pair_gmax);
   const int32_t r0 = m.shard(P0);
+  const bool bias_mma = kBias == kBiasMma && bias_on_mma(P, hh);
+  if constexpr (!kFp8 && kBias == kBiasMma) {
+    if (bias_mma)
+      fill_bias_blocks(sgen + C::kOffQext, sgen + C::kOffKext, P.slopes[hh] * kLog2e, (float)m.run_step(), P.c2);
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
@@ -623,9 +654,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(bar(kBarKFull + 0), 0, P.status, kKernFwdTc, kSiteKFull);
         if (ok) {
           tc::fence_after_sync();
-          issue_s<kFp8>(tmem, sbase, 0, 0);
+          issue_s<kFp8>(tmem, sbase, 0, 0, bias_mma);
           tc::mma_commit(bar(kBarSFull + 0));
-          issue_s<kFp8>(tmem, sbase, 1, 0);
+          issue_s<kFp8>(tmem, sbase, 1, 0, bias_mma);
           tc::mma_commit(bar(kBarSFull + 1));
           tc::mma_commit(bar(kBarKEmpty + 0));
         }
@@ -643,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = mbar_wait(bar(kBarKFull + ks), ((j + 1) / kStages) & 1, P.status, kKernFwdTc, kSiteKFull);
             if (!ok) break;
             tc::fence_after_sync();
-            issue_s<kFp8>(tmem, sbase, 0, ks);
+            issue_s<kFp8>(tmem, sbase, 0, ks, bias_mma);
             tc::mma_commit(bar(kBarSFull + 0));
           } else {
             tc::mma_commit(bar(kBarODone + 0));
@@ -654,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_pv<kFp8>(tmem, sbase, 1, vs, j > 0);
           tc::mma_commit(bar(kBarVEmpty + vs));
           if (more) {
-            issue_s<kFp8>(tmem, sbase, 1, ks);
+            issue_s<kFp8>(tmem, sbase, 1, ks, bias_mma);
             tc::mma_commit(bar(kBarSFull + 1));
             tc::mma_commit(bar(kBarKEmpty + ks));
           } else {
@@ -694,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t t_s = tmem + lane_off + X * 128;
     const uint32_t t_o = tmem + lane_off + 256 + X * 128;
     const float c2 = P.c2;
-    const bool alibi = P.slopes != nullptr;
+    const bool alibi = kBias != kBiasNone;
     const float slope2 = alibi ? P.slopes[hh] * kLog2e : 0.f;
     volatile int32_t* gtab = reinterpret_cast<volatile int32_t*>(sgen + C::kOffGtab) + warp * kBM;
 
@@ -712,9 +743,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ALiBi bias linear in the column (tile on one side of every query and its
       // positions arithmetic); kMasked: no bias, visible keys a prefix of the
       // columns; kGeneral: element by element.
+      // With the ALiBi column term on the tensor core the tile's scores already
+      // carry it, and the row part is an offset of the reference (below).
       const bool visible_all = tile_has_rows && tile.valid == kBM && (P.causal ? below : true);
-      const int kind = visible_all ? (!alibi ? kPlain : ((below || above) && tile.step != 0 ? kLinear : kGeneral))
-                                   : (!alibi && (tile.step != 0 || !P.causal) ? kMasked : kGeneral);
+      int kind;
+      if constexpr (kBias == kBiasNone)
+        kind = visible_all ? kPlain : (tile.step != 0 || !P.causal ? kMasked : kGeneral);
+      else if constexpr (kBias == kBiasMma)
+        kind = !bias_mma ? kGeneral : (visible_all ? kPlain : kMasked);  // (aligned: every step != 0)
+      else
+        kind = visible_all && (below || above) && tile.step != 0 ? kLinear : kGeneral;
+
       // kMasked: key u of the tile is visible to this row iff u <= lim (u < valid,
       // and under causal gk0 + step * u <= gi)
       int lim = -1;
@@ -779,19 +818,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Pass 1: the row max of this tile (log2 domain); pass 2: probabilities,
       // packed to bf16 pairs and stored over S columns that have already been read
       // (P column k holds scores 2k, 2k+1).
-      if (kind == kPlain || kind == kMasked) {
+      if (kBias != kBiasElem && (kind == kPlain || kind == kMasked)) {
         SRow sr;
         tc::tmem_ld128(t_s, sr);
         tc::tmem_wait_ld();
         if (kind == kMasked) mask_after(sr, lim);
-        const float mu = move_max(plain_max(sr, c2));
-        l += plain_probs<kFp8>(t_s, sr, mu, c2);
-      } else if (kind == kLinear) {
-        SRow sr;
-        tc::tmem_ld128(t_s, sr);
-        tc::tmem_wait_ld();
-        const float mu = move_max(linear_max(sr, c2, rc.base, rc.sl));
-        l += linear_probs<kFp8>(t_s, sr, mu, c2, rc.base, rc.sl);
+        const float pm = plain_max(sr, c2);
+        if constexpr (kBias == kBiasMma) {
+          // the row part slope2 * (g(column 64) - g_i) as an unevaluated sum (exact product)
+          const float dk = (float)(tile.gk0 + kBiasMid * tile.step - gi);
+          const float bhi = slope2 * dk;
+          const float blo = fmaf(slope2, dk, -bhi);
+          const float mu = move_max(pm + bhi);
+          l += plain_probs<kFp8>(t_s, sr, (mu - bhi) - blo, c2);
+        } else {
+          const float mu = move_max(pm);
+          l += plain_probs<kFp8>(t_s, sr, mu, c2);
+        }
+      } else if (kBias == kBiasElem && kind == kLinear) {
+        const float mu = move_max(tile_max<kLinear>(t_s, rc));
+        l += tile_probs<kLinear, kFp8>(t_s, mu, rc);
       } else {
         const float mu = move_max(tile_max<kGeneral>(t_s, rc));
         l += tile_probs<kGeneral, kFp8>(t_s, mu, rc);
@@ -851,7 +897,7 @@ bool fwd_tc_supported(int64_t S, int64_t D, int32_t dtype) {
 
 namespace {
 
-template <bool kFp8>
+template <bool kFp8, int kBias>
 cudaError_t launch_fwd_tc_t(const AttnArgs& a, void* o, float* lse, cudaStream_t st) {
   using C = FwdCfg<kFp8>;
   const int64_t BH = a.B * a.H;
@@ -873,6 +919,7 @@ cudaError_t launch_fwd_tc_t(const AttnArgs& a, void* o, float* lse, cudaStream_t
   // Heaviest pairs first under causal, where pairs hold consecutive positions (in
   // the strided layout every pair already has about the same work).
   p.heavy_first = p.aligned && a.causal && a.map.layout != RA_LAYOUT_STRIDED;
+  p.alibi_mma = kBias == kBiasMma;
   p.slopes = a.slopes;
   p.c2 = a.scale * a.qk_scale * kLog2e;
   p.o_scale = a.v_scale;
@@ -885,14 +932,14 @@ cudaError_t launch_fwd_tc_t(const AttnArgs& a, void* o, float* lse, cudaStream_t
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(fwd_tc_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(fwd_tc_kernel<kFp8, kBias>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)C::kSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t pairs = (a.S + 255) / 256;
   const int64_t blocks = pairs * BH;
   if (blocks > INT32_MAX) return cudaErrorInvalidValue;
-  fwd_tc_kernel<kFp8><<<(unsigned)blocks, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, p);
+  fwd_tc_kernel<kFp8, kBias><<<(unsigned)blocks, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, p);
   note_launch();
   return cudaGetLastError();
 }
@@ -900,7 +947,15 @@ cudaError_t launch_fwd_tc_t(const AttnArgs& a, void* o, float* lse, cudaStream_t
 }  // namespace
 
 cudaError_t launch_fwd_tc(const AttnArgs& a, void* o, float* lse, cudaStream_t st) {
-  return a.dtype == RA_E4M3 ? launch_fwd_tc_t<true>(a, o, lse, st) : launch_fwd_tc_t<false>(a, o, lse, st);
+  if (a.slopes == nullptr)
+    return a.dtype == RA_E4M3 ? launch_fwd_tc_t<true, kBiasNone>(a, o, lse, st)
+                              : launch_fwd_tc_t<false, kBiasNone>(a, o, lse, st);
+  if (a.dtype == RA_E4M3) return launch_fwd_tc_t<true, kBiasElem>(a, o, lse, st);
+  // the tensor core takes the column term when every visible key lies at or
+  // before its query (causal) and every tile's positions are arithmetic (aligned)
+  const bool aligned = (a.map.run() % 256) == 0;
+  return a.causal && aligned ? launch_fwd_tc_t<false, kBiasMma>(a, o, lse, st)
+                             : launch_fwd_tc_t<false, kBiasElem>(a, o, lse, st);
 }
 
 }  // namespace ra

@@ -212,3 +212,86 @@ def test_alibi_exponent_precision_far_from_the_diagonal():
     err_late = np.max(np.abs(np.array(late, dtype=np.float64) - ref))
     assert err_folded < 1e-4, err_folded            # relative error of 2^x below 1e-4
     assert err_late > 10 * err_folded, (err_late, err_folded)
+
+
+def _bf16_round(x):
+    """Round a float64 to the nearest bf16 value (ties to even), returned as float64."""
+    import torch
+    return float(torch.tensor(x, dtype=torch.float64).to(torch.bfloat16).to(torch.float64))
+
+
+def _column_term_parts(slope2, step, c2, u):
+    """The causal-ALiBi column term of key u in raw-score units, taken relative to
+    the tile's middle column, slope2*step*(u-64)/c2, as four successive bf16
+    roundings (what the K-side block of the extra K step holds); their exact sum
+    is what the tensor core adds to the score."""
+    rest = float(slope2) * float(step) * (u - 64) / float(c2)
+    parts = []
+    for _ in range(4):
+        p = _bf16_round(rest)
+        parts.append(p)
+        rest -= p
+    return parts
+
+
+def _mma_bias_exponents(raw, slope2, step, c2, dk, lim=127):
+    """The forward's log2 exponents on a causal ALiBi tile whose column term rides on
+    the Q K^T product: S'_u = raw_u + (sum of the four parts), one fp32 rounding;
+    the row term slope2 * dk (dk = position of column 64 minus the query's) split
+    exactly into bhi + blo; the reference mu = fl(max S' * c2 + bhi) over the
+    visible columns u <= lim; x_u = fl(S'_u c2 - fl(fl(mu - bhi) - blo))."""
+    s1 = np.array([np.float32(np.float64(r) + sum(_column_term_parts(slope2, step, c2, u)))
+                   for u, r in enumerate(raw)], dtype=np.float32)
+    dkf = _f32(dk)
+    bhi = np.float32(np.float64(slope2) * np.float64(dkf))
+    blo = np.float32(np.float64(slope2) * np.float64(dkf) - np.float64(bhi))  # exact remainder (fma)
+    mu = np.float32(np.float64(np.float32(np.float64(s1[:lim + 1].max()) * np.float64(c2))) + np.float64(bhi))
+    mub = np.float32(np.float64(np.float32(np.float64(mu) - np.float64(bhi))) - np.float64(blo))
+    x = np.array([np.float32(np.float64(s) * np.float64(c2) - np.float64(mub)) for s in s1])
+    exact = np.array([np.float64(r) * np.float64(c2) + np.float64(slope2) * (np.float64(dkf) + step * (u - 64))
+                      for u, r in enumerate(raw)]) - np.float64(mu)
+    return x.astype(np.float64), exact, mu, (bhi, blo)
+
+
+@pytest.mark.parametrize("step", [1, 16])
+def test_alibi_column_term_on_the_tensor_core(step):
+    """Causal ALiBi with the column term added by the tensor core: for the
+    steepest head of the page's slope formula (2^(-8/H) with H = 32) on a diagonal
+    tile, whose visible keys matter most, the exponents of every key that carries
+    weight (probability above 2^-64 of the row's reference) are within 1e-4 of
+    exact (a relative error below 7e-5 in the probability, against 2^-9 for the
+    bf16 rounding of P), with the token-strided step (16) as well."""
+    rng = np.random.default_rng(11)
+    slope2 = _f32(2.0 ** (-8.0 / 32) * LOG2E)
+    c2 = _f32(LOG2E / math.sqrt(128))
+    for trial in range(8):
+        raw = (rng.standard_normal(128) * 11.3).astype(np.float32)
+        for lim in (0, 40, 64, 100, 127):         # the query's column in the diagonal tile
+            x, exact, _, _ = _mma_bias_exponents(raw, slope2, step, c2, dk=(64 - lim) * step, lim=lim)
+            keep = exact[:lim + 1] > -64
+            err = np.max(np.abs(x[:lim + 1] - exact[:lim + 1])[keep])
+            assert err < 1e-4, (lim, err)
+
+
+def test_alibi_row_term_split_far_from_the_diagonal():
+    """A ring-step partial whose keys all lie far before the query (2^18 tokens):
+    the row term slope2 * (gk0 - g_i) is ~3e5 in log2 units.  Taken as an exact
+    two-float sum (fma remainder) it leaves the exponents within 1e-4 of exact;
+    with the remainder dropped they are off by up to half an ulp of 3e5 (~1e-2)."""
+    rng = np.random.default_rng(12)
+    slope2 = _f32(2.0 ** (-8.0 / 32) * LOG2E)
+    c2 = _f32(LOG2E / math.sqrt(128))
+    errs, errs_nolo = [], []
+    for trial in range(40):
+        raw = (rng.standard_normal(128) * 11.3).astype(np.float32)
+        dk = -(2 ** 18 - 256) - int(rng.integers(0, 4096))
+        x, exact, mu, (bhi, blo) = _mma_bias_exponents(raw, slope2, 1, c2, dk=dk)
+        keep = exact > -64
+        errs.append(np.max(np.abs(x - exact)[keep]))
+        # the same without the remainder of the row term
+        mub = np.float32(np.float64(mu) - np.float64(bhi))
+        s1 = x + np.float64(np.float32(np.float64(mu) - np.float64(bhi)) - np.float64(blo))  # S' * c2
+        x_nolo = np.array([np.float32(np.float64(s) - np.float64(mub)) for s in s1])
+        errs_nolo.append(np.max(np.abs(x_nolo - exact)[keep]))
+    assert max(errs) < 1e-4, max(errs)
+    assert max(errs_nolo) > 10 * max(errs), (max(errs_nolo), max(errs))

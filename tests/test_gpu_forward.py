@@ -29,11 +29,39 @@ def test_c1_full_fp32():
     _check_forward(W["C1"])
 
 
-@pytest.mark.parametrize("cfg,S,H", [("C2", 2048, 2), ("C3", 2048, 2), ("C4", 2048, 3), ("C5", 4096, 1)])
+@pytest.mark.parametrize("cfg,S,H", [("C2", 2048, 2), ("C3", 2048, 2), ("C4", 2048, 3), ("C4", 4096, 4),
+                                     ("C5", 4096, 1)])
 def test_bf16_reduced(cfg, S, H):
     """The bf16 configurations at a size the oracle finishes in seconds (same
-    layout and N, several tiles per shard)."""
+    layout and N, several tiles per shard).  C4 at S=2048 has 128-token chunks
+    (the per-element ALiBi path); at S=4096 its 256-token chunks take the path
+    that adds the ALiBi column term on the tensor core."""
     _check_forward(W[cfg], S=S, H=H)
+
+
+@pytest.mark.parametrize("layout,N,S,slopes", [
+    ("zigzag", 4, 2048, [0.9, 40.0, 2.0 ** -8]),   # head 1: too steep for the tensor-core term
+    ("strided", 8, 4096, [0.9, 3.0]),               # step 8: head 1 too steep
+    ("contiguous", 2, 1024, [1.0, -0.25]),          # a negative slope (a bias growing with distance)
+])
+def test_alibi_caller_slopes(layout, N, S, slopes):
+    """Causal ALiBi with slopes the caller chooses, including ones steep enough
+    that the kernel keeps the per-element bias for that head while the other
+    heads of the same launch add the column term on the tensor core."""
+    import context_ra_forward_gb300 as ra
+    H = len(slopes)
+    w = inputs.Workload("sl", 1, H, S, 128, "bf16", True, True, N, layout, False, 29)
+    x = inputs.make_inputs(w)
+    d = torch.device("cuda:0")
+    q, k, v = (ra.zigzag_permute(x[n].to(d), N, layout) for n in ("q", "k", "v"))
+    sl = torch.tensor(slopes, dtype=torch.float32)
+    o, lse = ra.forward(q, k, v, causal=True, alibi_slopes=sl.to(d), N=N, layout=layout)
+    perm, _ = oracle.index_maps(S, N, layout)
+    f = {n: inputs.to_f64_numpy(t) for n, t in x.items()}
+    o_ref, l_ref = oracle.attention_forward(f["q"], f["k"], f["v"], causal=True, scale=1.0 / math.sqrt(128),
+                                            slopes=sl.double().numpy())
+    compare(to_orig(o, perm), o_ref, "bf16", "O")
+    compare(to_orig(lse, perm), l_ref, "bf16", "LSE")
 
 
 RAGGED = [

@@ -19,6 +19,7 @@ CASES = [
     # (name, dtype, causal, alibi, N, layout, B, H, S, D)
     ("zz_causal", "bf16", True, False, 4, "zigzag", 1, 2, 2048, 128),
     ("st_alibi", "bf16", True, True, 4, "strided", 1, 2, 4096, 128),
+    ("zz_alibi", "bf16", True, True, 4, "zigzag", 1, 2, 4096, 128),   # 512-token chunks
     ("ct_noncausal", "bf16", False, False, 2, "contiguous", 1, 2, 1024, 128),
     ("f32_zz", "f32", True, True, 2, "zigzag", 1, 2, 1024, 64),
 ]
