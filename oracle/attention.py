@@ -61,7 +61,7 @@ def check_split(S: int, N: int, layout: str) -> None:
         raise ValueError(f"unknown layout {layout!r}")
     if N < 1 or S < 0:
         raise ValueError("need N >= 1 and S >= 0")
-    parts = N if layout == CONTIGUOUS else 2 * N
+    parts = 2 * N if layout == ZIGZAG else N  # 2N chunks; N equal pieces; tokens dealt out N at a time
     if S % parts:
         raise ValueError(f"S={S} is not divisible by {parts} ({layout}, N={N})")
 

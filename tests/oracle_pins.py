@@ -51,14 +51,16 @@ def _read_golden(name):
 # Index maps
 # ---------------------------------------------------------------------------
 def pin_index_golden(ora):
-    """Hand-written S=16 shard membership: N=2 contiguous / zig-zag ([CP] §2.1,
-    [ZZ] §Zig Zag) and the page's own token-strided example with N=4."""
-    for name, n in (("zigzag_S16_N2.txt", 2), ("strided_S16_N4.txt", 4)):
+    """Hand-written shard membership: S=16, N=2 contiguous / zig-zag ([CP] §2.1,
+    [ZZ] §Zig Zag) and the page's own token-strided example with N=4, at S=16 and
+    at S=12 (a multiple of N but not of 2N)."""
+    for name, S, n in (("zigzag_S16_N2.txt", 16, 2), ("strided_S16_N4.txt", 16, 4),
+                       ("strided_S12_N4.txt", 12, 4)):
         for line in _read_golden(name):
             head, toks = line.split(":")
             layout, r = head.split()
             want = [int(t) for t in toks.split()]
-            got = ora.shard_members(16, n, layout)[int(r)]
+            got = ora.shard_members(S, n, layout)[int(r)]
             assert got == want, (layout, r, got, want)
 
 

@@ -21,6 +21,7 @@ CASES = [
     ("strided_alibi", "bf16", True, True, 4, "strided", 1, 2, 2048, 128),
     ("strided_nc_alibi", "bf16", False, True, 2, "strided", 1, 1, 1024, 128),
     ("strided_ragged", "bf16", True, False, 3, "strided", 1, 2, 1200, 128),
+    ("strided_odd", "bf16", True, True, 4, "strided", 1, 2, 1292, 128),   # S % N == 0, S % 2N != 0
     # several batches and heads (per-(b, h) block order, per-head ALiBi slopes)
     ("batch_heads", "bf16", True, True, 2, "zigzag", 2, 3, 1024, 128),
     ("batch_heads_nc", "bf16", False, False, 4, "contiguous", 3, 2, 512, 128),

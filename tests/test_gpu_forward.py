@@ -85,6 +85,8 @@ RAGGED = [
     ("st_alibi", "bf16", True, True, 8, "strided", 1, 2, 4096, 128),
     ("st_nc_alibi", "bf16", False, True, 2, "strided", 1, 2, 1024, 128),
     ("st_ragged", "bf16", True, True, 3, "strided", 1, 2, 1200, 128),      # 400 slots: tiles straddle shards
+    ("st_odd", "bf16", True, True, 4, "strided", 1, 2, 1292, 128),         # S % N == 0, S % 2N != 0
+    ("st_odd_nc", "bf16", False, False, 4, "strided", 1, 2, 1292, 128),
     ("st_f32", "f32", True, True, 4, "strided", 1, 2, 512, 64),
 ]
 
