@@ -9,5 +9,5 @@ from .binding import (  # noqa: F401
     RAError, LAYOUTS, index_map, zigzag_permute, unpermute, forward, backward,
     backward_workspace_bytes, forward_path, check_device_status, debug_wait_timeout, lib,
     kernel_launch_count, backward_noalloc, noalloc_scratch_bytes, debug_wait_sites,
-    forward_ring_step, lse_merge, forward_fp8, rope_permute, rope_unpermute,
+    forward_ring_step, lse_merge, forward_fp8, rope_permute, rope_unpermute, shard_work,
 )

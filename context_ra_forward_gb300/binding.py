@@ -45,6 +45,8 @@ def lib() -> ctypes.CDLL:
     L = ctypes.CDLL(LIB_PATH)
     perm = [_vp, _vp, _i64, _i64, _i64, _i64, _i32, _i32, _i32, _vp]
     L.ra_index_map.argtypes = [_i64, _i32, _i32, _vp, _vp]
+    L.ra_shard_work.argtypes = [_i64, _i32, _i32, _i32, _vp, _vp, _vp]
+    L.ra_shard_work.restype = ctypes.c_int32
     L.ra_zigzag_permute.argtypes = perm
     L.ra_unpermute.argtypes = perm
     rope = [_vp, _vp, _i64, _i64, _i64, _i64, _i32, _i32, _i32, ctypes.c_double, _i64, _vp]
@@ -125,6 +127,15 @@ def index_map(S: int, N: int, layout: str):
     inv = np.empty(S, dtype=np.int64)
     _check(lib().ra_index_map(S, N, _layout(layout), perm.ctypes.data, inv.ctypes.data), "ra_index_map")
     return perm, inv
+
+
+def shard_work(S: int, N: int, layout: str, causal: bool = True):
+    """Per shard, for one head: (visible pairs, fully visible 128x128 tiles,
+    partially visible tiles), each an int64 numpy array of N entries."""
+    pairs, full, part = (np.empty(N, dtype=np.int64) for _ in range(3))
+    _check(lib().ra_shard_work(S, N, _layout(layout), int(bool(causal)), pairs.ctypes.data, full.ctypes.data,
+                               part.ctypes.data), "ra_shard_work")
+    return pairs, full, part
 
 
 def _permute(fn, x, N, layout, out, stream):
@@ -236,9 +247,11 @@ def kernel_launch_count() -> int:
 def backward_noalloc(q, k, v, o, lse, dout, *, causal=False, alibi_slopes=None, softmax_scale=None,
                      N=1, layout="contiguous", out=None, stream=None):
     """dQ, dK, dV through ra_backward_noalloc: the same backward, for callers that
-    cannot allocate device memory at this point (the library's own fixed scratch
-    buffer replaces the workspace, so problems larger than it are rejected).  The
-    outputs here are allocated by torch unless `out` supplies them."""
+    cannot allocate device memory at this point (a framework that owns every
+    allocation, memory fixed at start-up, a loop that cannot take an allocation's
+    synchronisation).  The library's own fixed scratch buffer replaces the
+    workspace, so problems larger than it are rejected.  The outputs here are
+    allocated by torch unless `out` supplies them."""
     B, H, S, D = _bhsd(q, "q")
     for t, n in ((k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
         if _bhsd(t, n) != q.shape or t.dtype != q.dtype:

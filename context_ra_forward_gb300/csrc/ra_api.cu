@@ -9,6 +9,7 @@
 
 #include <atomic>
 #include <mutex>
+#include <new>
 
 #include "ra_common.cuh"
 #include "ra_kernels.h"
@@ -193,6 +194,47 @@ ra_status ra_index_map(int64_t S, int32_t N, ra_layout layout, int64_t* perm_hos
   return RA_OK;
 }
 
+ra_status ra_shard_work(int64_t S, int32_t N, ra_layout layout, int32_t causal, int64_t* pairs_host,
+                        int64_t* tiles_full_host, int64_t* tiles_partial_host) {
+  if (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_ZIGZAG && layout != RA_LAYOUT_STRIDED)
+    return RA_ERR_UNSUPPORTED;
+  if (S < 0 || N < 1) return RA_ERR_INVALID_ARG;
+  const int64_t parts = layout == RA_LAYOUT_ZIGZAG ? 2 * (int64_t)N : (int64_t)N;
+  if (S % parts) return RA_ERR_INVALID_ARG;
+  if (S > (int64_t(1) << 22)) return RA_ERR_UNSUPPORTED;  // the tile count is quadratic in S
+  const ra::SeqMap m = ra::SeqMap::make(S, N, layout);
+  const int64_t c = m.c;
+  constexpr int64_t T = 128;
+  // global position ranges of the K/V tiles (128 slots of the shard-major buffer)
+  const int64_t nk = (S + T - 1) / T;
+  int64_t* kmin = new (std::nothrow) int64_t[nk > 0 ? nk : 1];
+  int64_t* kmax = new (std::nothrow) int64_t[nk > 0 ? nk : 1];
+  if (!kmin || !kmax) {
+    delete[] kmin;
+    delete[] kmax;
+    return RA_ERR_UNSUPPORTED;
+  }
+  for (int64_t b = 0; b < nk; ++b) m.grange(b * T, (b + 1) * T < S ? (b + 1) * T : S, kmin[b], kmax[b]);
+  for (int32_t r = 0; r < N; ++r) {
+    int64_t pairs = 0, full = 0, partial = 0;
+    for (int64_t p = r * c; p < (r + 1) * c; ++p) pairs += causal ? m.g(p) + 1 : S;
+    for (int64_t a = r * c; a < (r + 1) * c; a += T) {  // the shard's query tiles
+      int64_t qmin, qmax;
+      m.grange(a, a + T < (r + 1) * c ? a + T : (r + 1) * c, qmin, qmax);
+      for (int64_t b = 0; b < nk; ++b) {
+        if (!causal || kmax[b] <= qmin) ++full;
+        else if (kmin[b] <= qmax) ++partial;
+      }
+    }
+    if (pairs_host) pairs_host[r] = pairs;
+    if (tiles_full_host) tiles_full_host[r] = full;
+    if (tiles_partial_host) tiles_partial_host[r] = partial;
+  }
+  delete[] kmin;
+  delete[] kmax;
+  return RA_OK;
+}
+
 ra_status ra_zigzag_permute(const void* x, void* y, int64_t B, int64_t H, int64_t S, int64_t D,
                             ra_dtype dt, int32_t N, ra_layout layout, void* stream) {
   return permute_common(x, y, B, H, S, D, dt, N, layout, stream, false);
@@ -329,11 +371,14 @@ size_t ra_backward_workspace_bytes(int64_t B, int64_t H, int64_t S, int64_t D) {
   return dvec + dq;
 }
 
-ra_status ra_backward(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                      const void* dout, void* dq, void* dk, void* dv, void* workspace,
-                      size_t ws_bytes, int64_t B, int64_t H, int64_t S, int64_t D, ra_dtype dt,
-                      int32_t causal, const float* slopes, float scale, int32_t N,
-                      ra_layout layout, void* stream) {
+}  // extern "C"
+
+namespace ra {
+
+ra_status backward_precheck(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                            const void* dout, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t S,
+                            int64_t D, ra_dtype dt, const float* slopes, float scale, int32_t N,
+                            ra_layout layout) {
   ra_status s = check_sizes(B, H, S, D, dt, N, layout);
   if (s != RA_OK) return s;
   if (dt == RA_E4M3) return RA_ERR_UNSUPPORTED;  // 8-bit inputs need scales: ra_forward_fp8
@@ -344,6 +389,21 @@ ra_status ra_backward(const void* q, const void* k, const void* v, const void* o
   for (const void* p : in16)
     if (!aligned(p, 16)) return RA_ERR_MISALIGNED;
   if (!aligned(lse, 4) || (slopes && !aligned(slopes, 4))) return RA_ERR_MISALIGNED;
+  return RA_OK;
+}
+
+}  // namespace ra
+
+extern "C" {
+
+ra_status ra_backward(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                      const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                      size_t ws_bytes, int64_t B, int64_t H, int64_t S, int64_t D, ra_dtype dt,
+                      int32_t causal, const float* slopes, float scale, int32_t N,
+                      ra_layout layout, void* stream) {
+  ra_status s = ra::backward_precheck(q, k, v, o, lse, dout, dq, dk, dv, B, H, S, D, dt, slopes, scale, N, layout);
+  if (s != RA_OK) return s;
+  if (B == 0 || H == 0 || S == 0) return RA_OK;
   const size_t need = ra_backward_workspace_bytes(B, H, S, D);
   if (!workspace || ws_bytes < need) return RA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return RA_ERR_MISALIGNED;

@@ -28,6 +28,12 @@ struct AttnArgs {
 
 // ra_api.cu — counts every kernel launch the library makes (host side).
 void note_launch();
+// ra_api.cu — every check ra_backward makes before it looks at its workspace, in
+// the same order (sizes, dtype, scale, pointers, alignment): RA_OK or the error.
+ra_status backward_precheck(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                            const void* dout, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t S,
+                            int64_t D, ra_dtype dt, const float* slopes, float scale, int32_t N,
+                            ra_layout layout);
 
 // ra_permute.cu
 cudaError_t launch_permute(const void* x, void* y, int64_t BH, int64_t S, int64_t row_bytes,

@@ -2,12 +2,12 @@
 //
 // ra_backward needs a device workspace (the per-row term D_i and the fp32 dQ
 // accumulator) that the caller allocates.  Some callers cannot do that at the
-// point where they run the backward: code that is being recorded into a CUDA
-// graph (a cudaMalloc there is not captured and may synchronise the device),
-// plugins inside a host framework that owns every allocation and forbids
-// allocating on its behalf, and latency-critical loops where an allocation's
-// implicit synchronisation is not acceptable.  For them this file keeps a fixed
-// scratch buffer in device memory, sized at build time, that every call reuses.
+// point where they run the backward: plug-ins inside a host framework that owns
+// every device allocation and forbids allocating on its behalf, programs whose
+// device memory is laid out once at start-up, and latency-critical loops where an
+// allocation's implicit device synchronisation is not acceptable.  For them this
+// file keeps a fixed scratch buffer in device memory, sized at build time, that
+// every call reuses.
 //
 // The buffer is a file-scope __device__ array, so every GPU that loads the
 // library holds kScratchBytes of it until the process exits.  In host code the
@@ -54,13 +54,17 @@ ra_status ra_backward_noalloc(const void* q, const void* k, const void* v, const
                               int64_t B, int64_t H, int64_t S, int64_t D, ra_dtype dtype,
                               int32_t causal, const float* alibi_slopes, float softmax_scale,
                               int32_t N, ra_layout layout, void* stream) {
-  if (B < 0 || H < 0 || S < 0 || D < 0) return RA_ERR_INVALID_ARG;
+  // The arguments are checked exactly as ra_backward checks them, so an invalid
+  // call gets the error ra_backward would give; only then is the (now bounded)
+  // scratch requirement compared with the buffer.
+  ra_status s = ra::backward_precheck(q, k, v, o, lse, dout, dq, dk, dv, B, H, S, D, dtype, alibi_slopes,
+                                      softmax_scale, N, layout);
+  if (s != RA_OK) return s;
+  if (B == 0 || H == 0 || S == 0) return RA_OK;
   if (ra_backward_workspace_bytes(B, H, S, D) > kScratchBytes) return RA_ERR_WORKSPACE;
   void* scratch = nullptr;
-  if (B > 0 && H > 0 && S > 0) {
-    const ra_status s = scratch_address(&scratch);
-    if (s != RA_OK) return s;
-  }
+  s = scratch_address(&scratch);
+  if (s != RA_OK) return s;
   // The backward's pre-pass writes every D_i and zeroes the dQ accumulator before
   // the main kernel reads them, so whatever an earlier call left in the buffer
   // does not matter.  Nothing here allocates.

@@ -82,6 +82,25 @@ ra_status ra_index_map(int64_t S, int32_t N, ra_layout layout,
                        int64_t* perm_host, int64_t* inv_host);
 
 /*
+ * ra_shard_work — how the attention work of one head splits over the shards (host
+ * only): the balance the 2N-chunk assignment is for ([ZZ] §Zig Zag: under a
+ * causal mask the contiguous split leaves the last shard with far more visible
+ * pairs than the first; the interleaved one gives every shard the same work).
+ * For each shard r (arrays of N int64, caller-owned host memory; any may be NULL):
+ *   pairs_host[r]:         (query, key) pairs visible to the shard's queries
+ *                          (causal: sum over its queries of g + 1; else S per query);
+ *   tiles_full_host[r]:    128 x 128 tiles (the shard's 128-slot query tiles against
+ *                          the 128-slot key tiles of the shard-major buffer) whose
+ *                          every pair is visible;
+ *   tiles_partial_host[r]: tiles with some but not all pairs visible (the causal
+ *                          diagonals the kernels mask); fully masked tiles are skipped.
+ * Multiply by B*H for a whole problem.  Errors: as ra_index_map, plus
+ * RA_ERR_UNSUPPORTED for S > 2^22 (the tile count is quadratic in S).
+ */
+ra_status ra_shard_work(int64_t S, int32_t N, ra_layout layout, int32_t causal, int64_t* pairs_host,
+                        int64_t* tiles_full_host, int64_t* tiles_partial_host);
+
+/*
  * ra_zigzag_permute — y[b,h,p,:] = x[b,h,perm(p),:]: original order -> shard-major.
  * [ZZ] §Zig Zag ("the index logic is slightly more involved"), [CP] §2.1.
  *   x, y: device, [B,H,S,D] of `dtype`; must not overlap.  A bit-exact row copy.
@@ -246,10 +265,11 @@ ra_status ra_backward(const void* q, const void* k, const void* v, const void* o
 
 /*
  * ra_backward_noalloc — ra_backward for callers that cannot allocate device memory
- * when they run the backward (e.g. while recording a CUDA graph, inside a host
- * framework that owns every allocation, or in a loop that cannot afford an
- * allocation's implicit synchronisation).  The pages have no counterpart to this
- * call: it only changes where the backward's scratch lives.
+ * when they run the backward: a plug-in inside a host framework that owns every
+ * device allocation and lets no library allocate on its behalf, a program whose
+ * device memory is fixed once at start-up, or a latency-bound loop that cannot
+ * take an allocation's implicit device synchronisation.  The pages have no
+ * counterpart to this call: it only changes where the backward's scratch lives.
  *   Instead of a caller-provided workspace it uses a fixed scratch buffer inside
  * the library: RA_NOALLOC_SCRATCH_BYTES (32 MiB) of device memory that every GPU
  * which loads the library holds until the process exits.  Problems whose
@@ -258,7 +278,8 @@ ra_status ra_backward(const void* q, const void* k, const void* v, const void* o
  *   All other arguments, layouts, results and errors are those of ra_backward.
  * The call allocates nothing.  Its first call on a device looks up the buffer's
  * device address (once per device, with that device current), so make that first
- * call before any stream capture.  Every call reuses the same buffer: calls that
+ * call before any stream capture.  Argument errors are found before the size
+ * check, so an invalid call gets exactly the error ra_backward would give it.  Every call reuses the same buffer: calls that
  * may overlap on the GPU (different streams without ordering, or several host
  * threads) race on it and must be serialised by the caller.  The buffer keeps the
  * last call's contents; each call clears what it needs before using it.

@@ -158,3 +158,65 @@ def test_backward_validation(L):
     assert bw(q, k, v, o, lse, do, q, dk, dv, ws, need, *args) == -1            # dQ over Q
     assert bw(q, k, v, o, lse, do, dq, dk, dk, ws, need, *args) == -1           # dK over dV
     assert bw(q, k, v, o, lse, do, dq, dk, dv, ws, need, 1, 2, 1024, 128, 2, 1, None, F0, 4, 1, None) == -2
+
+
+def test_noalloc_backward_validation_matches_backward(L):
+    """ra_backward_noalloc answers an invalid call with the error ra_backward gives
+    for it, even when the problem is also too large for its scratch buffer; only a
+    valid problem beyond the buffer gets RA_ERR_WORKSPACE.  No CUDA call is made."""
+    q, k, v, o, lse, do, dq, dk, dv = (_p(n << 40) for n in range(1, 10))
+    nb = L.ra_backward_noalloc
+    big = (1, 64, 65536)   # needs ~2 GB of scratch
+    # (D, dtype, N, layout, scale) -> the error ra_backward returns for the same call
+    for D, dt, N, layout, scale, want in [(96, 1, 8, 1, F0, -2),      # D unsupported
+                                          (128, 7, 8, 1, F0, -2),     # dtype unknown
+                                          (128, 2, 8, 1, F0, -2),     # e4m3 (needs scales)
+                                          (128, 1, 8, 9, F0, -2),     # layout unknown
+                                          (128, 1, 0, 1, F0, -1),     # N < 1
+                                          (128, 1, 3, 1, F0, -1),     # S % 2N
+                                          (128, 1, 8, 1, ctypes.c_float(float("nan")), -1)]:
+        args = (*big, D, dt, 1, None, scale, N, layout, None)
+        assert nb(q, k, v, o, lse, do, dq, dk, dv, *args) == want, (D, dt, N, layout)
+        ws = _p(20 << 40)
+        assert L.ra_backward(q, k, v, o, lse, do, dq, dk, dv, ws, 1 << 40, *args) == want
+    # NULL and misaligned pointers, as ra_backward
+    assert nb(None, k, v, o, lse, do, dq, dk, dv, *big, 128, 1, 1, None, F0, 8, 1, None) == -1
+    assert nb(_p(8), k, v, o, lse, do, dq, dk, dv, *big, 128, 1, 1, None, F0, 8, 1, None) == -3
+    # a valid problem beyond the buffer
+    assert nb(q, k, v, o, lse, do, dq, dk, dv, *big, 128, 1, 1, None, F0, 8, 1, None) == -6
+    # an empty problem: nothing to do
+    assert nb(None, None, None, None, None, None, None, None, None, 1, 2, 0, 128, 1, 1, None, F0, 8, 1,
+              None) == 0
+
+
+@pytest.mark.parametrize("S,N,layout,causal", [(1024, 4, "zigzag", True), (1024, 4, "contiguous", True),
+                                               (1024, 4, "strided", True), (1200, 3, "zigzag", True),
+                                               (1300, 4, "strided", True), (512, 2, "zigzag", False)])
+def test_shard_work_pairs_match_oracle(L, S, N, layout, causal):
+    """The library's per-shard pair counts (from its closed-form map) equal the
+    oracle's (from its explicit chunk walk); the tiles cover every visible pair."""
+    from context_ra_forward_gb300 import binding
+    pairs, full, part = binding.shard_work(S, N, layout, causal)
+    want = oracle.causal_pairs_per_shard(S, N, layout) if causal else [S * (S // N)] * N
+    assert list(pairs) == list(want)
+    assert (full * 128 * 128 + part * 128 * 128 >= pairs).all()
+
+
+def test_shard_work_balance_at_the_workloads(L):
+    """Per-head tile counts at the causal 64K-token and 256K-token workloads,
+    worked out by hand: with 128-token tiles, query tile i sees i full key tiles
+    and one diagonal.  Contiguous 8 x 8192: shard r holds query tiles 64r..64r+63,
+    so sum_i i = 2016 for shard 0 and 30688 for shard 7.  Zig-zag 16 chunks of 4096:
+    shard r holds tiles 32r.. and 32(15-r).., 16352 for every shard.  Zig-zag 32
+    chunks of 8192 (N = 16): 131008 per shard.  The pair counts are the closed
+    forms c^2 r + c(c+1)/2 (contiguous) and h^2 (2N-1) + h(h+1) (zig-zag)."""
+    from context_ra_forward_gb300 import binding
+    pairs, full, part = binding.shard_work(65536, 8, "contiguous", True)
+    assert full[0] == 2016 and full[7] == 30688 and list(part) == [64] * 8
+    assert list(pairs) == [8192 ** 2 * r + 8192 * 8193 // 2 for r in range(8)]
+    pairs, full, part = binding.shard_work(65536, 8, "zigzag", True)
+    assert list(full) == [16352] * 8 and list(part) == [64] * 8
+    assert list(pairs) == [4096 ** 2 * 15 + 4096 * 4097] * 8
+    pairs, full, part = binding.shard_work(262144, 16, "zigzag", True)
+    assert list(full) == [131008] * 16 and list(part) == [128] * 16
+    assert list(pairs) == [8192 ** 2 * 31 + 8192 * 8193] * 16

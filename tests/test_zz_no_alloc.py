@@ -1,12 +1,14 @@
 """ra_backward_noalloc — the backward for callers that cannot allocate device
-memory when they run it (graph capture, frameworks that own all allocations,
-loops that cannot take an allocation's synchronisation).  It uses the library's
-fixed scratch buffer instead of a caller workspace.
+memory when they run it (a framework that owns every device allocation, memory
+fixed at start-up, loops that cannot take an allocation's synchronisation).  It
+uses the library's fixed scratch buffer instead of a caller workspace.
 
 The test calls it through the C ABI twice in a row and compares each result with
 the regular ra_backward (caller-provided workspace) on the same inputs, within
 the parity tolerance of the other tests; the second call also shows that what
-the first call left in the shared buffer does not leak into the next result.
+the first call left in the shared buffer does not leak into the next result, and
+that the call takes no device memory (free device memory is the same before and
+after it, with the outputs supplied by the caller).
 This file is collected last so that a run stopping at the first failure has run
 every other test first; it also passes on its own in a fresh process."""
 import ctypes
@@ -50,8 +52,15 @@ def test_noalloc_backward_matches_backward_twice(case):
     o, lse = ra.forward(q, k, v, causal=causal, alibi_slopes=sl, N=N, layout=layout)
     ref = ra.backward(q, k, v, o, lse, do, causal=causal, alibi_slopes=sl, N=N, layout=layout)
     assert ra.backward_workspace_bytes(B, H, S, D) <= ra.noalloc_scratch_bytes()
+    outs = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
     for call in range(2):
-        got = ra.backward_noalloc(q, k, v, o, lse, do, causal=causal, alibi_slopes=sl, N=N, layout=layout)
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info()[0]
+        got = ra.backward_noalloc(q, k, v, o, lse, do, causal=causal, alibi_slopes=sl, N=N, layout=layout,
+                                  out=outs)
+        torch.cuda.synchronize()
+        if call == 1:  # (the first call on a device may still load the library's device code)
+            assert torch.cuda.mem_get_info()[0] == free0, "the call took device memory"
         st, detail = ra.check_device_status()
         assert st == 0, detail
         for g, r, n in zip(got, ref, ("dQ", "dK", "dV")):
