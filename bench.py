@@ -39,7 +39,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="C5", choices=["C2", "C3", "C4", "C5", "C3S", "C5S"])
+    ap.add_argument("--workload", default="C5", choices=["C2", "C3", "C4", "C5", "C3S", "C3C", "C5S"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-side-configs", action="store_true")
@@ -92,12 +92,33 @@ def flops_of(w, backward=None):
     return fwd, bwd
 
 
+# GB300 dense bf16 tensor-core rate (fp32 accumulate) on NVIDIA's datasheet:
+# 2.25 PFLOP/s per GPU without sparsity.  Reported beside the measured peaks.
+NOMINAL_BF16_TFLOPS = 2250.0
+
+
 def measured_peaks():
+    """The machine's measured peaks (a STREAM-style copy; cuBLAS bf16 burst and
+    sustained).  Without that file: the earlier measurement on a GB300 that this
+    pool's profiling notes give as the fallback (6.8 TB/s; 1.9 PFLOP/s burst,
+    1.7 sustained), labelled "fallback"."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             return json.load(f), "measured"
     except (OSError, ValueError):
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def peak_fractions(tflops):
+    """A bf16 TFLOP/s figure against the sustained and burst peaks (measured, or
+    the fallback) and the datasheet's dense rate."""
+    peaks, kind = measured_peaks()
+    out = {}
+    for key, name in (("bf16_tflops_sustained", "sustained"), ("bf16_tflops", "burst")):
+        if peaks.get(key):
+            out[f"of_{kind}_{name}"] = round(tflops / peaks[key], 4)
+    out["of_nominal_dense"] = round(tflops / NOMINAL_BF16_TFLOPS, 4)
+    return out
 
 
 def source_hash(files):
@@ -349,7 +370,30 @@ def side_config(cfg, dev, iters=3):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / iters
     fwd, _ = flops_of(w, backward=False)
-    return {"forward_ms": round(ms, 3), "forward_tflops": round(fwd / ms / 1e9, 1)}
+    tf = fwd / ms / 1e9
+    return {"forward_ms": round(ms, 3), "forward_tflops": round(tf, 1), "frac": peak_fractions(tf)}
+
+
+def balance_config(cfgs, dev):
+    """The causal work of each shard in both layouts of the 64K-token workload
+    (per head, from the library's own map: visible pairs, fully visible and
+    diagonal 128 x 128 tiles) beside the forward time of each layout.  On one GPU
+    every layout keeps all SMs busy, so the times agree; the per-shard counts are
+    what sets a multi-device ring's step time (its slowest shard)."""
+    import context_ra_forward_gb300 as ra
+    from context_ra_forward_gb300 import inputs
+    res = {}
+    for c in cfgs:
+        w = inputs.WORKLOADS[c]
+        pairs, full, part = ra.shard_work(w.S, w.N, w.layout, w.causal)
+        tiles = full + part
+        res[w.layout] = {"workload": c, "pairs_per_shard": [int(x) for x in pairs],
+                         "tiles_full_per_shard": [int(x) for x in full],
+                         "tiles_diagonal_per_shard": [int(x) for x in part],
+                         "max_over_mean_tiles": round(float(tiles.max() / tiles.mean()), 4),
+                         "max_over_min_pairs": round(float(pairs.max() / pairs.min()), 4),
+                         "forward": side_config(c, dev)}
+    return res
 
 
 def fp8_config(cfg, dev, iters=3):
@@ -376,7 +420,10 @@ def fp8_config(cfg, dev, iters=3):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / iters
     fwd, _ = flops_of(w, backward=False)
-    return {"dtype": "e4m3", "forward_ms": round(ms, 3), "forward_tflops": round(fwd / ms / 1e9, 1)}
+    tf = fwd / ms / 1e9
+    # the e4m3 dense rate is twice the bf16 one: fractions against 2x the bf16 peaks
+    return {"dtype": "e4m3", "forward_ms": round(ms, 3), "forward_tflops": round(tf, 1),
+            "frac_of_2x_bf16": peak_fractions(tf / 2.0)}
 
 
 def rope_config(cfg, dev, iters=10):
@@ -551,6 +598,7 @@ def run_ours(args, w):
                 "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
                 "peak_kind": f"{peak_kind} HBM copy"}
 
+    roof["frac_other_peaks"] = (peak_fractions(achieved) if roof["bound"] == "tensor" else None)
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(path, w, args, step_flops, world)
@@ -560,6 +608,7 @@ def run_ours(args, w):
         for c in ("C2", "C3", "C4", "C3S"):
             if c != w.name:
                 side[c] = side_config(c, dev)
+        side["C3_shard_balance"] = balance_config(("C3", "C3C"), dev)
         side["C3_separate_partials"] = partials_config("C3", dev)
         side["C2_fp8"] = fp8_config("C2", dev)
         side["C3_fp8"] = fp8_config("C3", dev)
@@ -578,7 +627,8 @@ def run_ours(args, w):
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
                 "data": "synthetic (seeded N(0,1), rounded to bf16)", "config": workload_config(w),
                 "tokens_per_s": round(world * w.B * w.S / (ms * 1e-3), 1),
-                "pct_of_bf16_peak": round(100.0 * value / world / (peaks.get("bf16_tflops_sustained") or 1), 2),
+                "pct_of_bf16_peak": {k.replace("of_", ""): round(100.0 * v, 2)
+                                     for k, v in peak_fractions(value / world).items()},
                 "phase_ms": {p: round(t, 3) for p, t in phase.items()},
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
                 "gpu_launches_per_step": launches / args.steps, "clocks": clocks,

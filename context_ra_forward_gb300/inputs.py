@@ -52,6 +52,8 @@ WORKLOADS = {
     # the same causal workloads with the token-strided assignment the Zig-Zag
     # section prints ("GPU 0 gets tokens [0, 4, 8...]")
     "C3S": Workload("C3S", 1, 32, 65536, 128, "bf16", True, False, 8, "strided", False, 3),
+    # C3 with the contiguous split, the unbalanced layout the zig-zag one corrects
+    "C3C": Workload("C3C", 1, 32, 65536, 128, "bf16", True, False, 8, "contiguous", False, 3),
     "C5S": Workload("C5S", 1, 16, 262144, 128, "bf16", True, False, 16, "strided", True, 5),
 }
 

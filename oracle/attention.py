@@ -110,11 +110,12 @@ def causal_pairs_per_shard(S: int, N: int, layout: str) -> list[int]:
 # ----------------------------------------------------------------------------
 # Attention by definition
 # ----------------------------------------------------------------------------
-def _scores(qrows, k, rows, keys, scale, slope, causal):
-    """Scaled, biased, masked scores of query rows `rows` against keys `keys`."""
-    s = scale * (qrows @ k[keys].T)
-    dist = np.abs(rows[:, None] - keys[None, :]).astype(np.float64)
+def _scores(qrows, kkeys, rows, keys, scale, slope, causal):
+    """Scaled, biased, masked scores of query rows `rows` (vectors qrows) against
+    keys `keys` (vectors kkeys, i.e. k[keys])."""
+    s = scale * (qrows @ kkeys.T)
     if slope is not None:
+        dist = np.abs(rows[:, None] - keys[None, :]).astype(np.float64)
         s = s - slope * dist
     if causal:
         s = np.where(keys[None, :] <= rows[:, None], s, -np.inf)
@@ -152,13 +153,14 @@ def attention_forward(q, k, v, *, causal: bool, scale: float, slopes=None,
     for b in range(B):
         for h in range(H):
             slope = None if slopes is None else float(slopes[h])
+            kk, vk = k[b, h][keys], v[b, h][keys]
             for a in range(0, R, blk):
                 r = rows[a:a + blk]
-                s = _scores(q[b, h, r], k[b, h], r, keys, scale, slope, causal)
+                s = _scores(q[b, h, r], kk, r, keys, scale, slope, causal)
                 lse = _row_lse(s)
                 p = np.exp(s - np.where(np.isfinite(lse), lse, 0.0)[:, None])
                 p[~np.isfinite(lse)] = 0.0
-                O[b, h, a:a + len(r)] = p @ v[b, h][keys]
+                O[b, h, a:a + len(r)] = p @ vk
                 L[b, h, a:a + len(r)] = lse
     return O, L
 
@@ -179,7 +181,7 @@ def attention_backward(q, k, v, dout, *, causal: bool, scale: float, slopes=None
             Dvec = np.sum(dout[b, h] * O[b, h], axis=1)
             for a in range(0, S, blk):
                 r = np.arange(a, min(S, a + blk))
-                s = _scores(q[b, h, r], k[b, h], r, keys, scale, slope, causal)
+                s = _scores(q[b, h, r], k[b, h], r, keys, scale, slope, causal)  # keys: all, in order
                 lse = L[b, h, r]
                 p = np.exp(s - lse[:, None])
                 dp = dout[b, h, r] @ v[b, h].T
@@ -200,7 +202,7 @@ def backward_dq_rows(q, k, v, dout, rows, *, causal: bool, scale: float, slopes=
     for b in range(B):
         for h in range(H):
             slope = None if slopes is None else float(slopes[h])
-            s = _scores(q[b, h, rows], k[b, h], rows, keys, scale, slope, causal)
+            s = _scores(q[b, h, rows], k[b, h], rows, keys, scale, slope, causal)  # keys: all, in order
             p = np.exp(s - L[b, h][:, None])
             dp = dout[b, h, rows] @ v[b, h].T
             Dvec = np.sum(dout[b, h, rows] * O[b, h], axis=1)
@@ -224,7 +226,7 @@ def backward_dkdv_cols(q, k, v, dout, cols, *, causal: bool, scale: float, slope
             slope = None if slopes is None else float(slopes[h])
             for a in range(0, len(rows), blk):
                 r = rows[a:a + blk]
-                s = _scores(q[b, h, r], k[b, h], r, cols, scale, slope, causal)
+                s = _scores(q[b, h, r], k[b, h, cols], r, cols, scale, slope, causal)
                 p = np.exp(s - L[b, h, a:a + len(r)][:, None])
                 dp = dout[b, h, r] @ v[b, h, cols].T
                 Dvec = np.sum(dout[b, h, r] * O[b, h, a:a + len(r)], axis=1)
@@ -292,7 +294,7 @@ def online_softmax_rows(q, k, v, *, causal: bool, scale: float, slopes=None,
             acc = np.zeros((S, D))
             for j0 in range(0, S, block):
                 keys = np.arange(j0, min(S, j0 + block))
-                s = _scores(q[b, h], k[b, h], rows, keys, scale, slope, causal)
+                s = _scores(q[b, h], k[b, h][keys], rows, keys, scale, slope, causal)
                 m_new = np.maximum(m, s.max(axis=1))
                 ref = np.where(np.isfinite(m_new), m_new, 0.0)
                 alpha = np.where(np.isfinite(m), np.exp(m - ref), 0.0)

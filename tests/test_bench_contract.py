@@ -122,3 +122,18 @@ def test_flop_counts_are_the_published_convention():
         assert abs(b - bwd) <= 1e-3 * max(bwd, 1.0), name
     # the strided variants do the same work as their zig-zag twins
     assert bench.flops_of(inputs.WORKLOADS["C5S"]) == bench.flops_of(inputs.WORKLOADS["C5"])
+
+
+def test_peak_fractions_name_their_denominators(tmp_path, monkeypatch):
+    """Every fraction of a bf16 figure says which peak it divides by: the pool's
+    measured sustained and burst cuBLAS rates (or the labelled fallback when the
+    measurement is absent) and the datasheet's dense 2.25 PFLOP/s."""
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (tmp_path / "MEASURED_PEAKS.json").write_text('{"bf16_tflops": 2000.0, "bf16_tflops_sustained": 1600.0}')
+    f = bench.peak_fractions(1200.0)
+    assert f == {"of_measured_sustained": 0.75, "of_measured_burst": 0.6, "of_nominal_dense": round(1200 / 2250, 4)}
+    (tmp_path / "MEASURED_PEAKS.json").unlink()
+    f = bench.peak_fractions(1190.0)
+    assert f["of_fallback_sustained"] == 0.7 and f["of_fallback_burst"] == round(1190 / 1900, 4)

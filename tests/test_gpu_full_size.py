@@ -82,3 +82,20 @@ def test_full_size(cfg):
         dk = res["dk"].double()
         ratio = float(dk.sum(dim=2).norm() / dk.abs().sum(dim=2).norm())
         assert ratio < 1e-2, f"sum dK not ~0: ratio {ratio:.3e}"
+
+
+def test_long_accumulation_dkdv():
+    """dK and dV of keys that collect gradient from many query tiles, element by
+    element: the 64K-token causal zig-zag layout (N = 8, 16 chunks of 4096) with a
+    backward, one head; the 128 keys at global positions S-16384 .. S-16257 are seen
+    by 16384 queries each (128 query tiles), spread over both chunks of every
+    shard's second half.  Compared with the oracle's dK/dV columns, which recompute
+    those 16384 query rows in full."""
+    w = inputs.Workload("C3-backward", 1, 1, 65536, 128, "bf16", True, False, 8, "zigzag", True, 3)
+    x, res = _run(w)
+    scale = 1.0 / math.sqrt(w.D)
+    f = {n: inputs.to_f64_numpy(t) for n, t in x.items()}
+    cols = np.arange(w.S - 16384, w.S - 16384 + 128)
+    dk_ref, dv_ref = oracle.backward_dkdv_cols(f["q"], f["k"], f["v"], f["do"], cols, causal=True, scale=scale)
+    compare(res["dk"][:, :, cols].float().cpu().numpy().astype(np.float64), dk_ref, w.dtype, "dK, 16384 queries")
+    compare(res["dv"][:, :, cols].float().cpu().numpy().astype(np.float64), dv_ref, w.dtype, "dV, 16384 queries")

@@ -16,14 +16,14 @@ ORACLE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))
 SOURCES = ("attention.py", "rope.py")  # executed in this order into one mutant module
 
 MUTATIONS = {
-    "dropped_scale": ("s = scale * (qrows @ k[keys].T)", "s = (qrows @ k[keys].T)"),
+    "dropped_scale": ("s = scale * (qrows @ kkeys.T)", "s = (qrows @ kkeys.T)"),
     "alibi_sign": ("s = s - slope * dist", "s = s + slope * dist"),
     "diagonal_masked": ("keys[None, :] <= rows[:, None]", "keys[None, :] < rows[:, None]"),
     "zigzag_pairing": ("shards[r].extend(chunks[2 * N - 1 - r])", "shards[r].extend(chunks[N + r])"),
     "zigzag_order": ("shards[r].extend(chunks[r])\n            shards[r].extend(chunks[2 * N - 1 - r])",
                      "shards[r].extend(chunks[2 * N - 1 - r])\n            shards[r].extend(chunks[r])"),
-    "q_k_swapped": ("s = _scores(q[b, h, r], k[b, h], r, keys, scale, slope, causal)\n                lse = _row_lse(s)",
-                    "s = _scores(k[b, h, r], q[b, h], r, keys, scale, slope, causal)\n                lse = _row_lse(s)"),
+    "q_k_swapped": ("s = _scores(q[b, h, r], kk, r, keys, scale, slope, causal)\n                lse = _row_lse(s)",
+                    "s = _scores(k[b, h, r], q[b, h][keys], r, keys, scale, slope, causal)\n                lse = _row_lse(s)"),
     "lse_no_log": ("lse = safe + np.log(tot)", "lse = safe + tot"),
     "ds_missing_D": ("ds = p * (dp - Dvec[r][:, None])", "ds = p * dp"),
     "dk_unscaled": ("dk[b, h] += scale * (ds.T @ q[b, h, r])\n    return dq, dk, dv",
