@@ -48,6 +48,10 @@ def parse_args():
                     help="reference arm: oracle time budget over all warm-up and timed steps")
     ap.add_argument("--heads", type=int, default=None, help="override H (smaller case of the workload)")
     ap.add_argument("--seq", type=int, default=None, help="override S (smaller case of the workload)")
+    ap.add_argument("--shards", type=int, default=None, help="override N (smaller case of the workload)")
+    ap.add_argument("--phase", choices=["step", "forward", "forward_fp8"], default="step",
+                    help="step: the whole path (the benchmark line); forward / forward_fp8: only the "
+                         "forward kernel of the workload (bf16 or e4m3 inputs), one short JSON line")
     return ap.parse_args()
 
 
@@ -639,6 +643,51 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
+def run_forward_only(args, w, fp8):
+    """The forward kernel of one workload alone, on device-generated inputs (the
+    small cases the kernel profiles are taken on): W untimed launches, then K
+    timed ones; one JSON line with the mean time.  Single process."""
+    import context_ra_forward_gb300 as ra
+    from context_ra_forward_gb300 import inputs
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed)
+    shape = (w.B, w.H, w.S, w.D)
+    sl = inputs.alibi_slopes(w.H).to(dev) if w.alibi else None
+    if fp8:
+        xs = [torch.randn(shape, generator=g, device=dev) for _ in range(3)]
+        scales = [float(x.abs().max()) / inputs.E4M3_MAX for x in xs]
+        q, k, v = ((x / s).to(torch.float8_e4m3fn) for x, s in zip(xs, scales))
+        del xs
+
+        def call(o=None, lse=None):
+            return ra.forward_fp8(q, k, v, *scales, causal=w.causal, alibi_slopes=sl, N=w.N, layout=w.layout,
+                                  out=o, lse=lse)
+    else:
+        q, k, v = (torch.randn(shape, generator=g, device=dev).to(torch.bfloat16) for _ in range(3))
+
+        def call(o=None, lse=None):
+            return ra.forward(q, k, v, causal=w.causal, alibi_slopes=sl, N=w.N, layout=w.layout, out=o, lse=lse)
+    o, lse = call()
+    for _ in range(max(0, args.warmup - 1)):
+        call(o, lse)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        call(o, lse)
+    e1.record()
+    torch.cuda.synchronize()
+    st, detail = ra.check_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} {detail}")
+    ms = e0.elapsed_time(e1) / max(1, args.steps)
+    fwd, _ = flops_of(w, backward=False)
+    print(json.dumps({"phase": args.phase, "workload": workload_config(w)["workload"],
+                      "dtype": "e4m3" if fp8 else "bf16", "ms": round(ms, 4),
+                      "tflops": round(fwd / ms / 1e9, 1), "launches": args.warmup + args.steps}), flush=True)
+
+
 def run_e2e(path, w, args, step_flops, world):
     """Same step through the public API with HOST buffers: every step copies its
     inputs in from pinned host memory and its results (O, dQ, dK, dV in original
@@ -707,11 +756,13 @@ def main():
 
     from context_ra_forward_gb300 import inputs
     w = inputs.WORKLOADS[args.workload]
-    if args.heads or args.seq:
-        w = dataclasses.replace(w, H=args.heads or w.H, S=args.seq or w.S,
-                                name=f"{w.name}-small(H={args.heads or w.H},S={args.seq or w.S})")
+    if args.heads or args.seq or args.shards:
+        H, S, N = args.heads or w.H, args.seq or w.S, args.shards or w.N
+        w = dataclasses.replace(w, H=H, S=S, N=N, name=f"{w.name}-small(H={H},S={S},N={N})")
     if args.impl == "reference":
         run_reference(args, w)
+    elif args.phase != "step":
+        run_forward_only(args, w, fp8=args.phase == "forward_fp8")
     else:
         run_ours(args, w)
 
