@@ -89,3 +89,38 @@ def test_fp8_rejects():
     with pytest.raises(ra.RAError) as e:  # the plain entry point needs scales for e4m3
         ra.forward(q, q, q, N=1)
     assert e.value.status == -2
+
+
+@pytest.mark.parametrize("cfg", ["C2", "C3"])
+def test_fp8_full_size(cfg):
+    """The e4m3 forward at the full sizes the benchmark times (C2: non-causal
+    32K tokens x 32 heads, N=8 contiguous; C3: causal 64K tokens x 32 heads, N=8
+    zig-zag), on query rows from every shard of the first and last head, against
+    the oracle on the values the e4m3 inputs stand for.  Heads are independent, so
+    a head subset is exact parity on those heads."""
+    import context_ra_forward_gb300 as ra
+    w = inputs.WORKLOADS[cfg]
+    wf = inputs.Workload(cfg, w.B, w.H, w.S, w.D, "f32", w.causal, False, w.N, w.layout, False, w.seed)
+    x = inputs.make_inputs(wf)
+    q8 = {n: inputs.quantize_e4m3(x[n]) for n in ("q", "k", "v")}
+    del x
+    dev = torch.device("cuda:0")
+    dq = {n: ra.zigzag_permute(q8[n][0].to(dev), w.N, w.layout) for n in q8}
+    o, lse = ra.forward_fp8(dq["q"], dq["k"], dq["v"], q8["q"][1], q8["k"][1], q8["v"][1], causal=w.causal,
+                            N=w.N, layout=w.layout)
+    st, detail = ra.check_device_status()
+    assert st == 0, detail
+    del dq
+    perm, _ = oracle.index_maps(w.S, w.N, w.layout)
+    slots = np.linspace(0, w.S - 1, 48).astype(np.int64)
+    rows = np.unique(np.concatenate([perm[slots], [0, w.S - 1]]))
+    o_orig = ra.unpermute(o, w.N, w.layout)
+    lse_orig = to_orig(lse, perm)
+    for hh in sorted({0, w.H - 1}):
+        f = {n: inputs.dequantize_f64(q8[n][0][:, hh:hh + 1], q8[n][1]) for n in q8}
+        o_ref, l_ref = oracle.attention_forward(f["q"], f["k"], f["v"], causal=w.causal,
+                                                scale=1.0 / math.sqrt(w.D), rows=rows)
+        vmax = float(np.max(np.abs(f["v"])))
+        got = o_orig[:, hh:hh + 1, rows].float().cpu().numpy().astype(np.float64)
+        _check(got, o_ref, 2.0 ** -4 * vmax + 2e-2, f"{cfg} e4m3 head {hh} O rows")
+        compare(lse_orig[:, hh:hh + 1, rows], l_ref, "bf16", f"{cfg} e4m3 head {hh} LSE rows")
