@@ -10,4 +10,5 @@ from .binding import (  # noqa: F401
     backward_workspace_bytes, forward_path, check_device_status, debug_wait_timeout, lib,
     kernel_launch_count, backward_noalloc, noalloc_scratch_bytes, debug_wait_sites,
     forward_ring_step, lse_merge, forward_fp8, rope_permute, rope_unpermute, shard_work,
+    backward_path,
 )

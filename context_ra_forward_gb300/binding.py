@@ -62,6 +62,8 @@ def lib() -> ctypes.CDLL:
     L.ra_status_string.restype = ctypes.c_char_p
     L.ra_check_device_status.argtypes = [_vp, _vp]
     L.ra_forward_path.argtypes = [_i64, _i64, _i64, _i64, _i32, _i32, _i32]
+    L.ra_backward_path.argtypes = [_i64, _i64, _i64, _i64, _i32, _i32, _i32]
+    L.ra_backward_path.restype = ctypes.c_int32
     L.ra_debug_wait_timeout.argtypes = [_i32, _vp]
     L.ra_forward_fp8.argtypes = [_vp, _vp, _vp, _f32, _f32, _f32, _vp, _vp, _i64, _i64, _i64, _i64, _i32,
                                  _vp, _f32, _i32, _i32, _vp]
@@ -183,6 +185,12 @@ def rope_unpermute(x, N: int, layout: str = "zigzag", *, base: float = 10000.0, 
 def forward_path(B, H, S, D, dtype, N, layout) -> int:
     """1 = tensor-core kernel, 2 = CUDA-core fp32 kernel, 0 = empty, < 0 = rejected."""
     return lib().ra_forward_path(B, H, S, D, DTYPES[dtype], N, _layout(layout))
+
+
+def backward_path(B, H, S, D, dtype, N, layout) -> int:
+    """The kernel ra_backward runs (16-byte aligned LSE): 1 = tensor-core, 2 = CUDA-core
+    fp32, 0 = empty, < 0 = rejected."""
+    return lib().ra_backward_path(B, H, S, D, DTYPES[dtype], N, _layout(layout))
 
 
 def forward(q, k, v, *, causal=False, alibi_slopes=None, softmax_scale=None, N=1,

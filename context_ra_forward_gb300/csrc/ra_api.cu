@@ -265,6 +265,15 @@ int32_t ra_forward_path(int64_t B, int64_t H, int64_t S, int64_t D, ra_dtype dt,
   return ra::fwd_tc_supported(S, D, dt) ? 1 : 2;
 }
 
+int32_t ra_backward_path(int64_t B, int64_t H, int64_t S, int64_t D, ra_dtype dt, int32_t N,
+                         ra_layout layout) {
+  const ra_status s = check_sizes(B, H, S, D, dt, N, layout);
+  if (s != RA_OK) return s;
+  if (dt == RA_E4M3) return RA_ERR_UNSUPPORTED;
+  if (B == 0 || H == 0 || S == 0) return 0;
+  return ra::bwd_tc_supported(S, D, dt, ra::SeqMap::make(S, N, layout)) ? 1 : 2;
+}
+
 ra_status ra_forward(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
                      int64_t H, int64_t S, int64_t D, ra_dtype dt, int32_t causal,
                      const float* slopes, float scale, int32_t N, ra_layout layout, void* stream) {

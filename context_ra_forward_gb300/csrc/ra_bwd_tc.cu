@@ -130,14 +130,22 @@ struct BwdParams {
 };
 
 struct QTile {
-  int64_t p0;   // first shard-major slot
-  int64_t g0;   // its global position (tiles are contiguous)
+  int64_t p0;      // first shard-major slot
+  int64_t g0;      // its global position
+  int64_t g1;      // global position of column cb (when cb < valid)
+  int64_t gmin, gmax;
+  int32_t valid;   // columns below S
+  int32_t cb;      // columns 0..cb-1 are g0 + step*col, columns cb.. are g1 + step*(col - cb)
 };
 
-// Q tiles that see a K/V tile, in ring order; every 128-row tile lies inside one
-// run (a zig-zag chunk, or a shard otherwise, a multiple of 128 slots long), so
-// its global positions are g0, g0 + step, ... (step 1, or N when strided).
-template <bool kStrided>
+// Q tiles that see a K/V tile, in ring order.  Aligned shapes (every run a whole
+// number of 128-row tiles): every tile lies inside one run (a zig-zag chunk, or a
+// shard otherwise), so its global positions are g0, g0 + step, ... (step 1, or N
+// when strided).  Ragged shapes (kRagged: runs of at least 128 slots that are not
+// a multiple of 128): the tiles are the 128-slot tiles of the buffer owned by the
+// shard of their first row; such a tile holds at most one run boundary (two
+// arithmetic pieces), and the last one ends at S.
+template <bool kStrided, bool kRagged>
 struct QWalk {
   const BwdParams* P;
   int64_t kgmin;
@@ -157,6 +165,35 @@ struct QWalk {
   }
   __device__ bool next(QTile& out) {
     const SeqMap& m = P->map;
+    if constexpr (kRagged) {
+      while (true) {
+        while (ti >= tend) {
+          if (++t >= m.N) {
+            t = m.N;
+            return false;
+          }
+          const int32_t s = (s0 + t) % m.N;
+          ti = (s * m.c + kBM - 1) / kBM;
+          tend = ((s + 1) * m.c + kBM - 1) / kBM;
+        }
+        const int64_t p0 = ti * kBM;
+        ++ti;
+        const int64_t p1 = p0 + kBM < P->S ? p0 + kBM : P->S;
+        int64_t gmin, gmax;
+        m.grange(p0, p1, gmin, gmax);
+        if (P->causal && gmax < kgmin) continue;  // every query before every key
+        out.p0 = p0;
+        out.g0 = m.g(p0);
+        out.gmin = gmin;
+        out.gmax = gmax;
+        out.valid = (int32_t)(p1 - p0);
+        const int64_t run_end = (p0 / m.run() + 1) * m.run();
+        out.cb = m.layout != RA_LAYOUT_CONTIGUOUS && run_end - p0 < out.valid ? (int32_t)(run_end - p0)
+                                                                            : out.valid;
+        out.g1 = out.cb < out.valid ? m.g(p0 + out.cb) : 0;
+        return true;
+      }
+    }
     const int32_t nseg = m.layout == RA_LAYOUT_ZIGZAG ? 2 : 1;
     while (ti >= tend) {
       if (++seg >= nseg) {
@@ -192,6 +229,11 @@ struct QWalk {
     }
     out.p0 = seg_p0 + ti * kBM;
     out.g0 = seg_g0 + ti * kBM * step;
+    out.gmin = out.g0;
+    out.gmax = out.g0 + (kBM - 1) * step;
+    out.valid = kBM;
+    out.cb = kBM;
+    out.g1 = 0;
     ++ti;
     return true;
   }
@@ -203,8 +245,9 @@ enum TileKind { kPlain = 0, kLinear = 1, kGeneral = 2 };
 // q0g + step*col), log2 domain.
 struct ColCtx {
   float c2, slope2, lin_base, lin_sl;
-  int64_t gj, q0g, step;
-  bool causal, alibi;
+  int64_t gj, q0g, q1g, step;
+  int32_t cb, valid;  // the tile's column pieces and columns below S (as QTile)
+  bool causal, alibi, row_ok;
 };
 
 // col: query column within the tile; colh: the same within this warp's 64-column
@@ -217,8 +260,8 @@ __device__ __forceinline__ float prob(float s, float lse2, int col, int colh, co
   } else if constexpr (kKind == kLinear) {
     return tc::ex2(fmaf(s, c.c2, fmaf(c.lin_sl, (float)colh, c.lin_base) - lse2));
   } else {
-    const int64_t gi = c.q0g + c.step * col;
-    const bool vis = !c.causal || c.gj <= gi;
+    const int64_t gi = col < c.cb ? c.q0g + c.step * col : c.q1g + c.step * (col - c.cb);
+    const bool vis = c.row_ok && col < c.valid && (!c.causal || c.gj <= gi);
     float v = s * c.c2 - lse2;
     if (c.alibi) v -= c.slope2 * (float)(gi > c.gj ? gi - c.gj : c.gj - gi);
     return vis ? tc::ex2(v) : 0.f;
@@ -269,7 +312,7 @@ __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-template <bool kStrided>
+template <bool kStrided, bool kRagged>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -290,15 +333,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   // to one or two heads and share that head's Q/dO tiles and dQ rows in L2 (with
   // heads minor they spanned every head and the kernel ran at the DRAM roofline).
   const int64_t L = blockIdx.x;
-  const int64_t ntiles = S / kBM;
+  const int64_t ntiles = (S + kBM - 1) / kBM;
   const int64_t bh = L / ntiles;
   const int64_t tile = L - bh * ntiles;
   const int hh = (int)(bh % P.H);
   // (heaviest first under causal where tiles hold consecutive positions; strided
   // shards are balanced already)
-  const int64_t kp0 = P.causal && !kStrided ? m.inv(tile * kBM) : tile * kBM;
+  const int64_t kp0 = P.causal && !kStrided && !kRagged ? m.inv(tile * kBM) : tile * kBM;
   const int64_t kg0 = m.g(kp0);
   const int32_t s0 = m.shard(kp0);
+  // ragged: K/V rows below S, and the smallest and largest key position of the tile
+  const int32_t kvalid = kRagged ? (int32_t)(S - kp0 < kBM ? S - kp0 : kBM) : kBM;
+  int64_t kgmin_t = kg0, kgmax_t = kg0 + (kBM - 1) * (kStrided ? (int64_t)m.N : 1);
+  if constexpr (kRagged) m.grange(kp0, kp0 + kvalid, kgmin_t, kgmax_t);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
@@ -341,8 +388,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // each part is added to the accumulator with its own bulk reduce as soon as
       // the softmax warps have staged it.  The stage is refilled once both
       // reduces have read their sources and dK_i has read Q_i (Q first).
-      QWalk<kStrided> walk;
-      walk.init(&P, kg0, s0);
+      QWalk<kStrided, kRagged> walk;
+      walk.init(&P, kgmin_t, s0);
       QTile qt;
       int64_t stage_p0[2] = {0, 0};
       int loaded = 0;
@@ -396,8 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       const uint32_t kb = sbase + kOffK, vb = sbase + kOffV, dsb = sbase + kOffDS;
-      QWalk<kStrided> walk;
-      walk.init(&P, kg0, s0);
+      QWalk<kStrided, kRagged> walk;
+      walk.init(&P, kgmin_t, s0);
       QTile qt;
       bool ok = mbar_wait(bar(kBarKV), 0, P.status, kKernBwdTc, kSiteKFull);
       bool more = ok && walk.next(qt);
@@ -505,7 +552,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int krow = qd * 32 + lane;
     const uint32_t t_row = tmem + ((uint32_t)(qd * 32) << 16);
     const int64_t gstep = kStrided ? m.N : 1;  // compile-time 1 unless strided
-    const int64_t gj = kg0 + gstep * krow;     // K/V tiles are arithmetic runs
+    // aligned: K/V tiles are arithmetic runs; ragged: this row's own position
+    const bool krow_ok = krow < kvalid;
+    const int64_t gj = kRagged ? (krow_ok ? m.g(kp0 + krow) : 0) : kg0 + gstep * krow;
     const bool alibi = P.slopes != nullptr;
     const float slope2 = alibi ? P.slopes[hh] * kLog2e : 0.f;
     ColCtx cc;
@@ -515,24 +564,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     cc.step = gstep;
     cc.causal = P.causal != 0;
     cc.alibi = alibi;
+    cc.row_ok = krow_ok;
     uint8_t* ds_tile = sgen + kOffDS + h * kBoxBytes;
     const float* lse_bh = P.lse + bh * S;
     const float* dvec_bh = P.dvec + bh * S;
+    // 16-byte row loads need 16-byte aligned rows: always when S is a multiple of
+    // 128 (aligned shapes); ragged shapes check the head's offset
+    const bool rows16 = !kRagged || ((bh * S) & 3) == 0;
 
-    QWalk<kStrided> walk;
-    walk.init(&P, kg0, s0);
+    QWalk<kStrided, kRagged> walk;
+    walk.init(&P, kgmin_t, s0);
     QTile qt;
     int i = 0;
     bool ok = true;
     while (walk.next(qt)) {
       // Tile kind for this K/V row block against this Q tile.
-      const int64_t qgmin = qt.g0, qgmax = qt.g0 + (kBM - 1) * gstep;
-      const int64_t kgmin = kg0, kgmax = kg0 + (kBM - 1) * gstep;
+      const int64_t qgmin = qt.gmin, qgmax = qt.gmax;
+      const int64_t kgmin = kgmin_t, kgmax = kgmax_t;
       const bool below = kgmax <= qgmin;                 // every key at or before every query
       const bool above = !cc.causal && kgmin >= qgmax;   // every key at or after every query
-      const bool full = cc.causal ? below : (!alibi || below || above);
+      // (ragged: partial tiles and tiles with two position pieces take the per-element path)
+      const bool whole = !kRagged || (kvalid == kBM && qt.valid == kBM && qt.cb == kBM);
+      const bool full = whole && (cc.causal ? below : (!alibi || below || above));
       const int kind = full ? (alibi ? kLinear : kPlain) : kGeneral;
       cc.q0g = qt.g0;
+      cc.q1g = qt.g1;
+      cc.cb = qt.cb;
+      cc.valid = qt.valid;
       // bias of column col: below: -slope (q0g + col - gj); above: -slope (gj - q0g - col)
       cc.lin_sl = (below ? -slope2 : slope2) * (float)gstep;
       cc.lin_base = (below ? -slope2 * (float)(qt.g0 - gj) : -slope2 * (float)(gj - qt.g0)) +
@@ -540,10 +598,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // this tile's LSE row is loaded while S^T is computed (and its D row while dP^T is)
       float4 lva[16];
-      {
+      if (!kRagged || (qt.valid == kBM && rows16)) {
         const float4* lse_q = reinterpret_cast<const float4*>(lse_bh + qt.p0 + 64 * h);
 #pragma unroll
         for (int u = 0; u < 16; ++u) lva[u] = __ldg(lse_q + u);
+      } else {
+        // one column at a time; columns at or past S: an infinite LSE makes their
+        // probabilities 0
+        float lv[64];
+#pragma unroll
+        for (int u = 0; u < 64; ++u) {
+          const int col = 64 * h + u;
+          lv[u] = col < qt.valid ? __ldg(lse_bh + qt.p0 + col) : INFINITY;
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u) lva[u] = make_float4(lv[4 * u], lv[4 * u + 1], lv[4 * u + 2], lv[4 * u + 3]);
       }
       ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarSFull), i & 1, P.status, kKernBwdTc, kSiteSFull));
       if (!ok) break;
@@ -554,10 +623,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       else compute_p<kGeneral>(t_row, h, lva, cc, p);
       // the D row, loaded while dP^T is computed
       float4 dva[16];
-      {
+      if (!kRagged || (qt.valid == kBM && rows16)) {
         const float4* dv_q = reinterpret_cast<const float4*>(dvec_bh + qt.p0 + 64 * h);
 #pragma unroll
         for (int u = 0; u < 16; ++u) dva[u] = __ldg(dv_q + u);
+      } else {
+        float dl[64];
+#pragma unroll
+        for (int u = 0; u < 64; ++u) {
+          const int col = 64 * h + u;
+          dl[u] = col < qt.valid ? __ldg(dvec_bh + qt.p0 + col) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u) dva[u] = make_float4(dl[4 * u], dl[4 * u + 1], dl[4 * u + 2], dl[4 * u + 3]);
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
@@ -656,9 +734,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int u = 0; u < 16; ++u)
           pk[u] = tc::pack_bf16(__uint_as_float(r[2 * u]) * mul, __uint_as_float(r[2 * u + 1]) * mul);
-        uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+        if (krow_ok) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) d4[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          for (int u = 0; u < 4; ++u) d4[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
       }
     }
     tc::fence_before_sync();
@@ -686,7 +766,10 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
 }  // namespace
 
 bool bwd_tc_supported(int64_t S, int64_t D, int32_t dtype, const SeqMap& m) {
-  return dtype == RA_BF16 && D == kD && S >= kBM && m.run() % kBM == 0;
+  // aligned runs, or runs of at least one tile (a 128-slot tile then meets at most
+  // one run boundary); the contiguous layout is a single run of positions
+  const bool runs_ok = m.layout == RA_LAYOUT_CONTIGUOUS || m.run() >= kBM;
+  return dtype == RA_BF16 && D == kD && S >= kBM && runs_ok;
 }
 
 cudaError_t launch_bwd_tc(const AttnArgs& a, const float* lse, const void* dout, const float* dvec,
@@ -716,20 +799,26 @@ cudaError_t launch_bwd_tc(const AttnArgs& a, const float* lse, const void* dout,
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(bwd_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)kSmemBytes);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(bwd_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)kSmemBytes);
+    const void* kernels[] = {(const void*)bwd_tc_kernel<false, false>, (const void*)bwd_tc_kernel<true, false>,
+                             (const void*)bwd_tc_kernel<false, true>, (const void*)bwd_tc_kernel<true, true>};
+    for (const void* k : kernels)
+      if (attr_err == cudaSuccess)
+        attr_err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  const int64_t tiles = a.S / kBM;
+  const int64_t tiles = (a.S + kBM - 1) / kBM;
   const int64_t blocks = tiles * BH;
   if (blocks > INT32_MAX) return cudaErrorInvalidValue;
-  if (a.map.layout == RA_LAYOUT_STRIDED)
-    bwd_tc_kernel<true><<<(unsigned)blocks, kThreads, kSmemBytes, st>>>(tq, tk, tv, tdo, tdq, p);
+  const bool strided = a.map.layout == RA_LAYOUT_STRIDED;
+  const bool ragged = a.map.run() % kBM != 0;
+  if (!ragged && strided)
+    bwd_tc_kernel<true, false><<<(unsigned)blocks, kThreads, kSmemBytes, st>>>(tq, tk, tv, tdo, tdq, p);
+  else if (!ragged)
+    bwd_tc_kernel<false, false><<<(unsigned)blocks, kThreads, kSmemBytes, st>>>(tq, tk, tv, tdo, tdq, p);
+  else if (strided)
+    bwd_tc_kernel<true, true><<<(unsigned)blocks, kThreads, kSmemBytes, st>>>(tq, tk, tv, tdo, tdq, p);
   else
-    bwd_tc_kernel<false><<<(unsigned)blocks, kThreads, kSmemBytes, st>>>(tq, tk, tv, tdo, tdq, p);
+    bwd_tc_kernel<false, true><<<(unsigned)blocks, kThreads, kSmemBytes, st>>>(tq, tk, tv, tdo, tdq, p);
   note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

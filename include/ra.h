@@ -317,6 +317,19 @@ int32_t ra_forward_path(int64_t B, int64_t H, int64_t S, int64_t D, ra_dtype dty
                         int32_t N, ra_layout layout);
 
 /*
+ * ra_backward_path — which kernel ra_backward would run for these arguments, given
+ * a 16-byte aligned LSE (the tensor-core kernel reads LSE and D rows 16 bytes at a
+ * time): 1 = tensor-core (tcgen05) kernel, 2 = CUDA-core fp32 kernel, 0 = nothing
+ * to do, a negative ra_status if the arguments would be rejected.  The tensor-core
+ * kernel takes bf16 with D = 128 and S >= 128 when each run of consecutive
+ * positions (a zig-zag chunk or a strided shard) is at least 128 slots long, so a
+ * 128-slot tile meets at most one run boundary; the contiguous layout is one run.
+ * Host only, no launch.
+ */
+int32_t ra_backward_path(int64_t B, int64_t H, int64_t S, int64_t D, ra_dtype dtype,
+                         int32_t N, ra_layout layout);
+
+/*
  * ra_debug_wait_sites — after ra_check_device_status reported a failure: for the
  * block that failed first, what each of its warps was waiting on when its wait
  * gave up, one int32 per warp (site << 24 | parity << 16 | low 16 bits of the

@@ -82,6 +82,13 @@ def test_forward_path_and_validation(L):
     assert fwd(vp, vp, vp, ctypes.c_void_p(1 << 20), vp, 1, 2, 64, 100, 1, 1, None, ctypes.c_float(0.0), 4, 1, None) == -2
     mis = ctypes.c_void_p(8)
     assert fwd(mis, vp, vp, ctypes.c_void_p(1 << 20), vp, 1, 2, 64, 128, 1, 1, None, ctypes.c_float(0.0), 4, 1, None) == -3
+    bp = L.ra_backward_path
+    assert bp(1, 2, 1200, 128, 1, 3, 1) == 1      # 200-token chunks: tensor cores
+    assert bp(1, 2, 1000, 128, 1, 4, 0) == 1      # contiguous, ragged tail
+    assert bp(1, 2, 512, 128, 1, 4, 1) == 2       # 64-token chunks: CUDA cores
+    assert bp(1, 2, 1024, 128, 0, 4, 1) == 2      # fp32
+    assert bp(1, 2, 1024, 128, 2, 4, 1) == -2     # e4m3 has no backward
+    assert bp(1, 2, 1000, 128, 1, 3, 1) == -1     # 1000 % 6
     # permute: aliasing input and output is rejected
     assert L.ra_zigzag_permute(vp, vp, 1, 1, 64, 128, 1, 4, 1, None) == -1
 

@@ -18,6 +18,7 @@ CASES = [
     (16384, 4, 8, "strided", True, False),
     (8192, 4, 4, "contiguous", True, True),
     (8192, 2, 2, "zigzag", False, False),
+    (1200, 2, 3, "zigzag", True, True),     # ragged runs: 200-token chunks on the tensor cores
 ]
 
 
