@@ -122,7 +122,7 @@ struct FwdParams {
   int32_t causal;
   int32_t aligned;      // every 256-row query pair and 128-row tile lies in one run
   int32_t heavy_first;  // causal + aligned: CTAs ordered by decreasing work
-  int32_t alibi_mma;    // causal + aligned + ALiBi + bf16: the column term rides on the Q K^T product
+  int32_t head_filter;  // 0: every head; 1: only heads whose column term fits the tensor core; 2: only the others
   const float* slopes;
   float c2;             // softmax scale * log2(e) (for e4m3: times the Q and K scales)
   float o_scale;        // V scale (1 for bf16)
@@ -437,14 +437,14 @@ __device__ __forceinline__ float tile_probs(uint32_t t_s, float mu, const RowCtx
 // halves its largest magnitude, slope2 * step * 64 in log2 units.  The fp32 score
 // accumulator holds the term to about 2^-24 of that; up to kMaxMmaColumnTerm
 // (≈ 1.2e-4 in the exponent, far below the bf16 rounding of P) the tensor core
-// carries it, and steeper slopes keep the per-element path.
+// carries it.  Heads with steeper slopes run in a second launch of the
+// per-element form (launch_fwd_tc).
 constexpr int kBiasMid = 64;
 constexpr float kMaxMmaColumnTerm = 2048.0f;
 
-// Whether this CTA's head carries its ALiBi column term on the Q K^T product
-// (every role evaluates the same expression on the same inputs).
-__device__ __forceinline__ bool bias_on_mma(const FwdParams& P, int hh) {
-  if (!P.alibi_mma) return false;
+// Whether head hh's ALiBi column term can ride on the Q K^T product (every CTA of
+// both launches of a causal ALiBi forward evaluates the same expression).
+__device__ __forceinline__ bool column_term_fits(const FwdParams& P, int hh) {
   const float t = fabsf(P.slopes[hh] * kLog2e) * (float)P.map.run_step() * (float)kBiasMid;
   return t <= kMaxMmaColumnTerm;  // false for NaN slopes too
 }
@@ -567,7 +567,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   int64_t pair_gmin, pair_gmax;
   m.grange(P0, qend, pair_gmin, pair_gmax);
   const int32_t r0 = m.shard(P0);
-  const bool bias_mma = kBias == kBiasMma && bias_on_mma(P, hh);
+  // A causal ALiBi forward runs as two launches: the tensor-core form for the heads
+  // whose column term fits, the per-element form for the rest; each CTA of the
+  // other launch's heads returns at once (the whole block, before any barrier).
+  if (P.head_filter != 0 && (P.head_filter == 1) != column_term_fits(P, hh)) return;
+  const bool bias_mma = kBias == kBiasMma;
   if constexpr (!kFp8 && kBias == kBiasMma) {
     if (bias_mma)
       fill_bias_blocks(sgen + C::kOffQext, sgen + C::kOffKext, P.slopes[hh] * kLog2e, (float)m.run_step(), P.c2);
@@ -750,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (kBias == kBiasNone)
         kind = visible_all ? kPlain : (tile.step != 0 || !P.causal ? kMasked : kGeneral);
       else if constexpr (kBias == kBiasMma)
-        kind = !bias_mma ? kGeneral : (visible_all ? kPlain : kMasked);  // (aligned: every step != 0)
+        kind = visible_all ? kPlain : kMasked;  // (aligned: every step != 0)
       else
         kind = visible_all && (below || above) && tile.step != 0 ? kLinear : kGeneral;
 
@@ -838,7 +842,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if (kBias == kBiasElem && kind == kLinear) {
         const float mu = move_max(tile_max<kLinear>(t_s, rc));
         l += tile_probs<kLinear, kFp8>(t_s, mu, rc);
-      } else {
+      } else if constexpr (kBias != kBiasMma) {
         const float mu = move_max(tile_max<kGeneral>(t_s, rc));
         l += tile_probs<kGeneral, kFp8>(t_s, mu, rc);
       }
@@ -898,7 +902,7 @@ bool fwd_tc_supported(int64_t S, int64_t D, int32_t dtype) {
 namespace {
 
 template <bool kFp8, int kBias>
-cudaError_t launch_fwd_tc_t(const AttnArgs& a, void* o, float* lse, cudaStream_t st) {
+cudaError_t launch_fwd_tc_t(const AttnArgs& a, void* o, float* lse, cudaStream_t st, int32_t head_filter = 0) {
   using C = FwdCfg<kFp8>;
   const int64_t BH = a.B * a.H;
   if (BH > INT32_MAX) return cudaErrorInvalidValue;
@@ -919,7 +923,7 @@ cudaError_t launch_fwd_tc_t(const AttnArgs& a, void* o, float* lse, cudaStream_t
   // Heaviest pairs first under causal, where pairs hold consecutive positions (in
   // the strided layout every pair already has about the same work).
   p.heavy_first = p.aligned && a.causal && a.map.layout != RA_LAYOUT_STRIDED;
-  p.alibi_mma = kBias == kBiasMma;
+  p.head_filter = head_filter;
   p.slopes = a.slopes;
   p.c2 = a.scale * a.qk_scale * kLog2e;
   p.o_scale = a.v_scale;
@@ -954,8 +958,10 @@ cudaError_t launch_fwd_tc(const AttnArgs& a, void* o, float* lse, cudaStream_t s
   // the tensor core takes the column term when every visible key lies at or
   // before its query (causal) and every tile's positions are arithmetic (aligned)
   const bool aligned = (a.map.run() % 256) == 0;
-  return a.causal && aligned ? launch_fwd_tc_t<false, kBiasMma>(a, o, lse, st)
-                             : launch_fwd_tc_t<false, kBiasElem>(a, o, lse, st);
+  if (!(a.causal && aligned)) return launch_fwd_tc_t<false, kBiasElem>(a, o, lse, st);
+  // heads whose column term fits the tensor core, then (per element) the others
+  const cudaError_t e = launch_fwd_tc_t<false, kBiasMma>(a, o, lse, st, 1);
+  return e != cudaSuccess ? e : launch_fwd_tc_t<false, kBiasElem>(a, o, lse, st, 2);
 }
 
 }  // namespace ra
