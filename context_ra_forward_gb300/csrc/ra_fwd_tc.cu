@@ -532,11 +532,13 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t sbase, int X, i
 
 // How a kernel instantiation adds the ALiBi bias: not at all (no slopes), on the
 // tensor core (causal, aligned, bf16: see the header), or per element in the
-// softmax (every other case).  Each instantiation holds only the tile paths its
-// case uses, which keeps the softmax warps' registers within their budget.
+// softmax (every other case).  kAligned (every 256-row query pair and 128-row tile
+// in one run of arithmetic positions) drops the per-element path from the
+// unbiased instantiation.  Each instantiation holds only the tile paths its case
+// uses, which keeps the softmax warps' registers and code within their budget.
 enum BiasMode { kBiasNone = 0, kBiasMma = 1, kBiasElem = 2 };
 
-template <bool kFp8, int kBias>
+template <bool kFp8, int kBias, bool kAligned>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ FwdParams P) {
@@ -752,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool visible_all = tile_has_rows && tile.valid == kBM && (P.causal ? below : true);
       int kind;
       if constexpr (kBias == kBiasNone)
-        kind = visible_all ? kPlain : (tile.step != 0 || !P.causal ? kMasked : kGeneral);
+        kind = visible_all ? kPlain : (kAligned || tile.step != 0 || !P.causal ? kMasked : kGeneral);
       else if constexpr (kBias == kBiasMma)
         kind = visible_all ? kPlain : kMasked;  // (aligned: every step != 0)
       else
@@ -842,7 +844,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if (kBias == kBiasElem && kind == kLinear) {
         const float mu = move_max(tile_max<kLinear>(t_s, rc));
         l += tile_probs<kLinear, kFp8>(t_s, mu, rc);
-      } else if constexpr (kBias != kBiasMma) {
+      } else if constexpr (kBias != kBiasMma && !(kBias == kBiasNone && kAligned)) {
         const float mu = move_max(tile_max<kGeneral>(t_s, rc));
         l += tile_probs<kGeneral, kFp8>(t_s, mu, rc);
       }
@@ -901,7 +903,7 @@ bool fwd_tc_supported(int64_t S, int64_t D, int32_t dtype) {
 
 namespace {
 
-template <bool kFp8, int kBias>
+template <bool kFp8, int kBias, bool kAligned>
 cudaError_t launch_fwd_tc_t(const AttnArgs& a, void* o, float* lse, cudaStream_t st, int32_t head_filter = 0) {
   using C = FwdCfg<kFp8>;
   const int64_t BH = a.B * a.H;
@@ -936,14 +938,14 @@ cudaError_t launch_fwd_tc_t(const AttnArgs& a, void* o, float* lse, cudaStream_t
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(fwd_tc_kernel<kFp8, kBias>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(fwd_tc_kernel<kFp8, kBias, kAligned>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)C::kSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t pairs = (a.S + 255) / 256;
   const int64_t blocks = pairs * BH;
   if (blocks > INT32_MAX) return cudaErrorInvalidValue;
-  fwd_tc_kernel<kFp8, kBias><<<(unsigned)blocks, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, p);
+  fwd_tc_kernel<kFp8, kBias, kAligned><<<(unsigned)blocks, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, p);
   note_launch();
   return cudaGetLastError();
 }
@@ -951,17 +953,23 @@ cudaError_t launch_fwd_tc_t(const AttnArgs& a, void* o, float* lse, cudaStream_t
 }  // namespace
 
 cudaError_t launch_fwd_tc(const AttnArgs& a, void* o, float* lse, cudaStream_t st) {
-  if (a.slopes == nullptr)
-    return a.dtype == RA_E4M3 ? launch_fwd_tc_t<true, kBiasNone>(a, o, lse, st)
-                              : launch_fwd_tc_t<false, kBiasNone>(a, o, lse, st);
-  if (a.dtype == RA_E4M3) return launch_fwd_tc_t<true, kBiasElem>(a, o, lse, st);
+  // aligned: every 256-row query pair and 128-row tile lies in one run of arithmetic
+  // positions, so the unbiased instantiation needs no per-element path
+  const bool aligned = (a.map.run() % 256) == 0;
+  if (a.slopes == nullptr) {
+    if (a.dtype == RA_E4M3)
+      return aligned ? launch_fwd_tc_t<true, kBiasNone, true>(a, o, lse, st)
+                     : launch_fwd_tc_t<true, kBiasNone, false>(a, o, lse, st);
+    return aligned ? launch_fwd_tc_t<false, kBiasNone, true>(a, o, lse, st)
+                   : launch_fwd_tc_t<false, kBiasNone, false>(a, o, lse, st);
+  }
+  if (a.dtype == RA_E4M3) return launch_fwd_tc_t<true, kBiasElem, false>(a, o, lse, st);
   // the tensor core takes the column term when every visible key lies at or
   // before its query (causal) and every tile's positions are arithmetic (aligned)
-  const bool aligned = (a.map.run() % 256) == 0;
-  if (!(a.causal && aligned)) return launch_fwd_tc_t<false, kBiasElem>(a, o, lse, st);
+  if (!(a.causal && aligned)) return launch_fwd_tc_t<false, kBiasElem, false>(a, o, lse, st);
   // heads whose column term fits the tensor core, then (per element) the others
-  const cudaError_t e = launch_fwd_tc_t<false, kBiasMma>(a, o, lse, st, 1);
-  return e != cudaSuccess ? e : launch_fwd_tc_t<false, kBiasElem>(a, o, lse, st, 2);
+  const cudaError_t e = launch_fwd_tc_t<false, kBiasMma, true>(a, o, lse, st, 1);
+  return e != cudaSuccess ? e : launch_fwd_tc_t<false, kBiasElem, false>(a, o, lse, st, 2);
 }
 
 }  // namespace ra
