@@ -311,7 +311,7 @@ __device__ __forceinline__ float plain_probs(uint32_t t_s, const SRow& sr, float
     }
     return (ls2[0].x + ls2[1].x) + (ls2[0].y + ls2[1].y);
   } else {
-    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+    float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
       uint32_t pk[16];
@@ -324,13 +324,14 @@ __device__ __forceinline__ float plain_probs(uint32_t t_s, const SRow& sr, float
                                      make_float2(c2, c2), make_float2(-mu, -mu));
           const float2 x1 = tc::fma2(make_float2(__uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3])),
                                      make_float2(c2, c2), make_float2(-mu, -mu));
-          const float pv[4] = {tc::ex2(x0.x), tc::ex2(x0.y), tc::ex2(x1.x), tc::ex2(x1.y)};
-          ls[u & 3] += (pv[0] + pv[1]) + (pv[2] + pv[3]);
-          pk[8 * ci + u] = tc::pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
+          const float2 p0 = make_float2(tc::ex2(x0.x), tc::ex2(x0.y));
+          const float2 p1 = make_float2(tc::ex2(x1.x), tc::ex2(x1.y));
+          ls2[u & 1] = tc::add2(ls2[u & 1], tc::add2(p0, p1));
+          pk[8 * ci + u] = tc::pack_e4m3x4(p0.x, p0.y, p1.x, p1.y);
         }
       tc::tmem_st16(t_s + 16 * hf, pk);
     }
-    return (ls[0] + ls[1]) + (ls[2] + ls[3]);
+    return (ls2[0].x + ls2[1].x) + (ls2[0].y + ls2[1].y);
   }
 }
 
