@@ -30,7 +30,11 @@
 // tensor core (one more K = 16 step of the Q K^T product against a fixed block:
 // ones for Q, the column term split into four bf16 parts for K), and the row
 // constant is an offset of the row's reference; the tiles then take the register
-// path of unbiased tiles.
+// path of unbiased tiles.  Heads whose slope makes that term too large for the
+// fp32 accumulator run in a second launch with the bias added per element.
+// The kernel is a template over the element type, the bias mode (none, tensor
+// core, per element) and whether every tile lies in one run of arithmetic
+// positions (aligned); each instantiation holds only the tile paths it can meet.
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512),
 // all fp32 with row i in lane i.  The softmax writes P (bf16 pairs) over the
 // first 64 columns of its S tile, and the PV product reads it from there.
