@@ -125,7 +125,7 @@ struct FwdParams {
   int32_t BH;
   int32_t causal;
   int32_t aligned;      // every 256-row query pair and 128-row tile lies in one run
-  int32_t heavy_first;  // causal + aligned: CTAs ordered by decreasing work
+  int32_t heavy_first;  // causal + aligned: CTAs ordered by decreasing work (1: by position, 2: strided)
   int32_t head_filter;  // 0: every head; 1: only heads whose column term fits the tensor core; 2: only the others
   const float* slopes;
   float c2;             // softmax scale * log2(e) (for e4m3: times the Q and K scales)
@@ -575,7 +575,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t bh = L / npairs;
   const int64_t pair = L - bh * npairs;
   const int hh = (int)(bh % P.H);
-  const int64_t P0 = P.heavy_first ? m.inv(S - 256 * (pair + 1)) : 256 * pair;
+  // Heaviest pairs first under causal.  Consecutive positions (zig-zag, contiguous):
+  // the pair holding the latest 256 positions first.  Token-strided: every shard's
+  // slots hold increasing positions, so pair k takes shard k mod N's (k div N)-th
+  // pair from the end.
+  int64_t P0 = 256 * pair;
+  if (P.heavy_first == 1) P0 = m.inv(S - 256 * (pair + 1));
+  else if (P.heavy_first == 2) P0 = (pair % m.N) * m.c + m.c - 256 * (pair / m.N + 1);
   const int64_t qend = P0 + 256 < S ? P0 + 256 : S;
   int64_t pair_gmin, pair_gmax;
   m.grange(P0, qend, pair_gmin, pair_gmax);
@@ -935,7 +941,7 @@ cudaError_t launch_fwd_tc_t(const AttnArgs& a, void* o, float* lse, cudaStream_t
   p.aligned = (a.map.run() % 256) == 0;
   // Heaviest pairs first under causal, where pairs hold consecutive positions (in
   // the strided layout every pair already has about the same work).
-  p.heavy_first = p.aligned && a.causal && a.map.layout != RA_LAYOUT_STRIDED;
+  p.heavy_first = !(p.aligned && a.causal) ? 0 : (a.map.layout == RA_LAYOUT_STRIDED ? 2 : 1);
   p.head_filter = head_filter;
   p.slopes = a.slopes;
   p.c2 = a.scale * a.qk_scale * kLog2e;
