@@ -18,8 +18,10 @@
 // warpgroups 200 registers and the third 104):
 //   warps 0-7  "softmax": warp w owns K/V rows 32*(w%4).. (its TMEM lane quarter)
 //              and Q columns 64*(w/4)..: P^T, dS^T, the dQ drain, the dK/dV epilogue
-//   warp  8    TMA producer: K and V once, then Q and dO tiles into a 2-stage ring;
-//              it also issues the bulk reduce-adds of each Q tile's dQ partial
+//   warp  8    TMA producer: K and V once, then Q and dO tiles into a 2-stage ring
+//              (aligned shapes: with each tile's LSE and D rows, so that no softmax
+//              warp waits on a global load); it also issues the bulk reduce-adds of
+//              each Q tile's dQ partial
 //   warp  9    TMEM allocation and MMA issue (one thread); warps 10-11 idle
 // TMEM (512 columns): S^T [0,128), dP^T [128,256), dK [256,384), dV [384,512);
 // all fp32 with K/V row r in lane r.  Each softmax warp writes P^T (bf16 pairs)
@@ -38,11 +40,13 @@
 // half of the tile's stage (which dV_i has read), both as soon as dQ_i is
 // complete.  The next tile's dS pass waits for the first reduce to have read the
 // dS^T tile; the Q half is refilled once dK_i has read it.  A post-pass scales
-// and converts the sums.  The LSE and D rows of a Q tile are loaded from global
-// memory before the waits they would otherwise follow.
+// and converts the sums.  The LSE and D rows of a Q tile reach shared memory by
+// bulk copies (ragged shapes: the softmax warps load them from global memory
+// before the waits they would otherwise follow).
 #include <cuda.h>
 #include <math.h>
 #include <mutex>
+#include <type_traits>
 
 #include "ra_common.cuh"
 #include "ra_kernels.h"
@@ -74,7 +78,12 @@ constexpr uint32_t kOffV = kOffK + kTileBytes;
 constexpr uint32_t kOffQ = kOffV + kTileBytes;        // 2 stages of [Q | dO]
 constexpr uint32_t kStageBytes = 2 * kTileBytes;
 constexpr uint32_t kOffDS = kOffQ + 2 * kStageBytes;  // dS^T, 32 KB
-constexpr uint32_t kOffBar = kOffDS + kTileBytes;
+// LSE rows of the Q tiles of both stages (512 B each), then one D row (the dS pass
+// of a tile reads it; each half is refilled once its four warps have drained)
+constexpr uint32_t kRowBytes = kBM * 4;
+constexpr uint32_t kOffLse = kOffDS + kTileBytes;
+constexpr uint32_t kOffDrow = kOffLse + 2 * kRowBytes;
+constexpr uint32_t kOffBar = kOffDrow + kRowBytes;
 enum Bar {
   kBarKV = 0,
   kBarQFull = 1,    // + stage: the Q half of the stage is loaded
@@ -101,7 +110,8 @@ enum Bar {
   kBarDQEmpty,
   kBarFinal,
   kBarEpiDone,  // every softmax warp has finished reading TMEM (count 8)
-  kNumBars
+  kBarDRow,     // + half: the D row of the next tile's columns 64*half.. is loaded
+  kNumBars = kBarDRow + 2
 };
 constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemUsed = kOffTmemSlot + 16;
@@ -270,9 +280,21 @@ __device__ __forceinline__ float prob(float s, float lse2, int col, int colh, co
 
 // P^T for this warp's 64 query columns: from S^T in TMEM into registers (fp32)
 // and back into TMEM as bf16 pairs for the dV product.
-template <int kKind>
-// lva: the 64 LSE values of these columns, loaded before S^T was waited for.
-__device__ __forceinline__ void compute_p(uint32_t t_row, int h, const float4 (&lva)[16], const ColCtx& c,
+// Row values (LSE or D) of this warp's 64 query columns, four at a time: held in
+// registers (loaded from global memory ahead of use), or read from the shared-memory
+// row where each is needed.
+struct RowsInRegs {
+  float4 v[16];
+  __device__ __forceinline__ float4 operator()(int q) const { return v[q]; }
+};
+struct RowsInSmem {
+  const float4* s;
+  __device__ __forceinline__ float4 operator()(int q) const { return s[q]; }
+};
+
+template <int kKind, typename Rows>
+// lse4(q): the LSE values of columns 4q..4q+3 of this warp's half.
+__device__ __forceinline__ void compute_p(uint32_t t_row, int h, const Rows& lse4, const ColCtx& c,
                                           float (&p)[64]) {
   uint32_t rr[2][32];
   tc::tmem_ld64(t_row + kColS + 64 * h, rr);
@@ -280,10 +302,10 @@ __device__ __forceinline__ void compute_p(uint32_t t_row, int h, const float4 (&
 #pragma unroll
   for (int ci = 0; ci < 2; ++ci) {
     const uint32_t (&r)[32] = rr[ci];
-    const float4* lv = lva + 8 * ci;
 #pragma unroll
     for (int u = 0; u < 32; u += 2) {
-      const float l4[4] = {lv[u >> 2].x, lv[u >> 2].y, lv[u >> 2].z, lv[u >> 2].w};
+      const float4 lq = lse4(8 * ci + (u >> 2));
+      const float l4[4] = {lq.x, lq.y, lq.z, lq.w};
       if constexpr (kKind == kGeneral) {
         p[32 * ci + u] = prob<kKind>(__uint_as_float(r[u]), l4[u & 3] * kLog2e, 64 * h + 32 * ci + u, 32 * ci + u, c);
         p[32 * ci + u + 1] = prob<kKind>(__uint_as_float(r[u + 1]), l4[(u + 1) & 3] * kLog2e,
@@ -306,6 +328,14 @@ __device__ __forceinline__ void compute_p(uint32_t t_row, int h, const float4 (&
 #pragma unroll
   for (int u = 0; u < 32; ++u) pk[u] = tc::pack_bf16(p[2 * u], p[2 * u + 1]);
   tc::tmem_st32(t_row + kColS + 64 * h, pk);
+}
+
+// Bulk copy without a tensor map: `bytes` (a multiple of 16) from 16-byte aligned
+// global memory into 16-byte aligned shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
 }
 
 __device__ __forceinline__ void fence_async_smem() {
@@ -393,11 +423,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       QTile qt;
       int64_t stage_p0[2] = {0, 0};
       int loaded = 0;
+      // Aligned shapes: the tile's LSE row comes with its Q tile (same barrier), and
+      // its D row into the one D buffer by halves, each once the four warps that
+      // read that half for the previous tile have drained it.
+      const float* lse_bh = P.lse + bh * S;
+      const float* dvec_bh = P.dvec + bh * S;
+      int drows[2] = {0, 0};  // D row halves loaded
       auto load_half = [&](const CUtensorMap* tm, int st, uint32_t off, int b, int64_t p0) {
         const uint32_t dst = sbase + kOffQ + st * kStageBytes + off;
-        mbar_arrive_expect_tx(bar(b + st), kTileBytes);
+        const bool lse_row = !kRagged && b == kBarQFull;
+        mbar_arrive_expect_tx(bar(b + st), kTileBytes + (lse_row ? kRowBytes : 0));
         for (int hf = 0; hf < 2; ++hf)
           tc::tma_load_3d(dst + hf * kBoxBytes, tm, hf * 64, (int32_t)p0, z, bar(b + st));
+        if (lse_row) bulk_load(sbase + kOffLse + st * kRowBytes, lse_bh + p0, kRowBytes, bar(b + st));
+      };
+      auto load_drow = [&](int half, int64_t p0) {
+        mbar_arrive_expect_tx(bar(kBarDRow + half), kRowBytes / 2);
+        bulk_load(sbase + kOffDrow + half * (kRowBytes / 2), dvec_bh + p0 + 64 * half, kRowBytes / 2,
+                  bar(kBarDRow + half));
+        ++drows[half];
       };
       mbar_arrive(bar(kBarDPFull));  // tile 0 has no predecessor
       for (int st = 0; st < 2 && walk.next(qt); ++st) {
@@ -406,16 +450,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         stage_p0[st] = qt.p0;
         ++loaded;
       }
+      if (!kRagged && loaded > 0) {
+        load_drow(0, stage_p0[0]);
+        load_drow(1, stage_p0[0]);
+      }
       for (int i = 0; i < loaded; ++i) {
         const int st = i & 1;
         const uint32_t src = sbase + kOffQ + st * kStageBytes;
         // dQ columns 0..63 from the dS^T tile first (the next tile's dS pass waits
         // for that read), then 64..127 from the dO half; Q_{i+2} once dK_i has read Q_i
         if (!mbar_wait(bar(kBarDrainQ + st), (i >> 1) & 1, P.status, kKernBwdTc, kSiteBwd)) break;
+        if (!kRagged && i + 1 < loaded) load_drow(0, stage_p0[(i + 1) & 1]);
         for (int b = 0; b < 2; ++b)  // 128-row x 32-column fp32 boxes
           tc::tma_reduce_add_3d(&tm_dq, sbase + kOffDS + b * kBoxBytes, 32 * b, (int32_t)stage_p0[st], z);
         tc::bulk_commit();
         if (!mbar_wait(bar(kBarDrainDO + st), (i >> 1) & 1, P.status, kKernBwdTc, kSiteBwd)) break;
+        if (!kRagged && i + 1 < loaded) load_drow(1, stage_p0[(i + 1) & 1]);
         for (int b = 2; b < 4; ++b)
           tc::tma_reduce_add_3d(&tm_dq, src + b * kBoxBytes, 32 * b, (int32_t)stage_p0[st], z);
         tc::bulk_commit();
@@ -439,6 +489,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(bar(kBarQFull + (ii & 1)), (ii >> 1) & 1, P.status, kKernBwdTc, kSiteQFull);
         mbar_wait(bar(kBarDOFull + (ii & 1)), (ii >> 1) & 1, P.status, kKernBwdTc, kSiteQFull);
       }
+      for (int hf = 0; hf < 2; ++hf)
+        if (drows[hf] > 0) mbar_wait(bar(kBarDRow + hf), (drows[hf] - 1) & 1, P.status, kKernBwdTc, kSiteQFull);
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
@@ -597,11 +649,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     cc.lin_sl * (float)(64 * h);  // this warp's first column
 
       // this tile's LSE row is loaded while S^T is computed (and its D row while dP^T is)
-      float4 lva[16];
-      if (!kRagged || (qt.valid == kBM && rows16)) {
+      // the LSE row: aligned shapes read it from shared memory as it is needed (the
+      // producer loaded it with the Q tile); ragged ones load it into registers from
+      // global memory while S^T is computed
+      std::conditional_t<kRagged, RowsInRegs, RowsInSmem> lse4;
+      if constexpr (!kRagged) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarQFull + (i & 1)), (i >> 1) & 1, P.status, kKernBwdTc,
+                                               kSiteQFull));
+        if (!ok) break;
+        lse4.s = reinterpret_cast<const float4*>(sgen + kOffLse + (i & 1) * kRowBytes) + 16 * h;
+      } else if (qt.valid == kBM && rows16) {
         const float4* lse_q = reinterpret_cast<const float4*>(lse_bh + qt.p0 + 64 * h);
 #pragma unroll
-        for (int u = 0; u < 16; ++u) lva[u] = __ldg(lse_q + u);
+        for (int u = 0; u < 16; ++u) lse4.v[u] = __ldg(lse_q + u);
       } else {
         // one column at a time; columns at or past S: an infinite LSE makes their
         // probabilities 0
@@ -612,35 +672,44 @@ __global__ void __launch_bounds__(kThreads, 1)
           lv[u] = col < qt.valid ? __ldg(lse_bh + qt.p0 + col) : INFINITY;
         }
 #pragma unroll
-        for (int u = 0; u < 16; ++u) lva[u] = make_float4(lv[4 * u], lv[4 * u + 1], lv[4 * u + 2], lv[4 * u + 3]);
+        for (int u = 0; u < 16; ++u) lse4.v[u] = make_float4(lv[4 * u], lv[4 * u + 1], lv[4 * u + 2], lv[4 * u + 3]);
       }
       ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarSFull), i & 1, P.status, kKernBwdTc, kSiteSFull));
       if (!ok) break;
       tc::fence_after_sync();
       float p[64];
-      if (kind == kPlain) compute_p<kPlain>(t_row, h, lva, cc, p);
-      else if (kind == kLinear) compute_p<kLinear>(t_row, h, lva, cc, p);
-      else compute_p<kGeneral>(t_row, h, lva, cc, p);
-      // the D row, loaded while dP^T is computed
-      float4 dva[16];
-      if (!kRagged || (qt.valid == kBM && rows16)) {
-        const float4* dv_q = reinterpret_cast<const float4*>(dvec_bh + qt.p0 + 64 * h);
+      if (kind == kPlain) compute_p<kPlain>(t_row, h, lse4, cc, p);
+      else if (kind == kLinear) compute_p<kLinear>(t_row, h, lse4, cc, p);
+      else compute_p<kGeneral>(t_row, h, lse4, cc, p);
+      // the D row (ragged shapes: from global memory, loaded while dP^T is computed)
+      std::conditional_t<kRagged, RowsInRegs, RowsInSmem> d4;
+      if constexpr (kRagged) {
+        if (qt.valid == kBM && rows16) {
+          const float4* dv_q = reinterpret_cast<const float4*>(dvec_bh + qt.p0 + 64 * h);
 #pragma unroll
-        for (int u = 0; u < 16; ++u) dva[u] = __ldg(dv_q + u);
-      } else {
-        float dl[64];
+          for (int u = 0; u < 16; ++u) d4.v[u] = __ldg(dv_q + u);
+        } else {
+          float dl[64];
 #pragma unroll
-        for (int u = 0; u < 64; ++u) {
-          const int col = 64 * h + u;
-          dl[u] = col < qt.valid ? __ldg(dvec_bh + qt.p0 + col) : 0.f;
+          for (int u = 0; u < 64; ++u) {
+            const int col = 64 * h + u;
+            dl[u] = col < qt.valid ? __ldg(dvec_bh + qt.p0 + col) : 0.f;
+          }
+#pragma unroll
+          for (int u = 0; u < 16; ++u) d4.v[u] = make_float4(dl[4 * u], dl[4 * u + 1], dl[4 * u + 2], dl[4 * u + 3]);
         }
-#pragma unroll
-        for (int u = 0; u < 16; ++u) dva[u] = make_float4(dl[4 * u], dl[4 * u + 1], dl[4 * u + 2], dl[4 * u + 3]);
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarPReady));
+      if constexpr (!kRagged) {
+        // aligned shapes: from shared memory, loaded by the producer once the previous
+        // tile's dS pass had read the buffer
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarDRow + h), i & 1, P.status, kKernBwdTc, kSiteQFull));
+        if (!ok) break;
+        d4.s = reinterpret_cast<const float4*>(sgen + kOffDrow) + 16 * h;
+      }
 
       // dS^T = P^T o (dP^T - D) into TMEM and shared memory (bf16, 128-byte
       // swizzle), once dP^T_i is complete and the reduce-add has read the previous
@@ -653,12 +722,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t r[32];
         tc::tmem_ld32(t_row + kColDP + 64 * h + 32 * ci, r);
         tc::tmem_wait_ld();
-        const float4* dvv = dva + 8 * ci;
         uint32_t dsk[16];  // dS^T of these 32 columns as bf16 pairs
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int u = 2 * e;
-          const float d0[4] = {dvv[u >> 2].x, dvv[u >> 2].y, dvv[u >> 2].z, dvv[u >> 2].w};
+          const float4 dq = d4(8 * ci + (u >> 2));
+          const float d0[4] = {dq.x, dq.y, dq.z, dq.w};
           // P o (dP - D) for the column pair, in packed fp32 pairs
           const float2 diff = tc::fma2(make_float2(d0[u & 3], d0[(u + 1) & 3]), make_float2(-1.f, -1.f),
                                        make_float2(__uint_as_float(r[u]), __uint_as_float(r[u + 1])));
