@@ -648,7 +648,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       cc.lin_base = (below ? -slope2 * (float)(qt.g0 - gj) : -slope2 * (float)(gj - qt.g0)) +
                     cc.lin_sl * (float)(64 * h);  // this warp's first column
 
-      // this tile's LSE row is loaded while S^T is computed (and its D row while dP^T is)
       // the LSE row: aligned shapes read it from shared memory as it is needed (the
       // producer loaded it with the Q tile); ragged ones load it into registers from
       // global memory while S^T is computed
