@@ -9,8 +9,8 @@ arrival counts and phases; a wait names the phase it is meant for.  TMA loads,
 reduce-adds and MMAs are asynchronous engines with random durations; the MMA
 commits arrive when every MMA issued before them has finished.  Every read and
 write of a buffer region (TMEM columns per half and lane quarter, the shared-
-memory dS^T tile, the Q and dO halves of each stage) is recorded with its time
-interval.
+memory dS^T tile, the Q and dO halves of each stage, the LSE row of each stage and
+the two halves of the one D row) is recorded with its time interval.
 
 Checked, over many random timings and tile counts:
   * every wait ends (no deadlock);
@@ -21,7 +21,8 @@ Checked, over many random timings and tile counts:
   * every read sees the version it needs (the dS pass reads dP^T of its own tile,
     the reduce-add reads the staged dQ of its own tile, ...).
 Planted mistakes in the model (a barrier shared by both stages, a staging buffer
-reused too early, a missing wait) must be caught.
+reused too early, a missing wait, the next D row loaded before the drains) must be
+caught.
 
 Failure paths: with a wait that never completes injected at every wait of every
 role in turn, the roles take the kernel's error exits; every role must still
@@ -66,22 +67,40 @@ def producer(sim, n, mut):
     if "dpfull_no_producer" not in mut:
         yield ("arrive", "DPFull")  # tile 0 has no predecessor
     loaded = 0
+    drows = [0, 0]  # D row halves loaded
+
+    def load_drow(half, tile):
+        drows[half] += 1
+        return ("load", [(("D", half), f"D{tile}")], f"DRow{half}")
+
     for st in range(min(2, n)):
-        yield ("load", [(("Q", st), f"Q{st}")], f"QFull{st}")
+        # the LSE row of the tile comes with its Q tile, on the same barrier
+        yield ("load", [(("Q", st), f"Q{st}"), (("LSE", st), f"L{st}")], f"QFull{st}")
         yield ("load", [(res, f"DO{st}") for res, _ in DO_all(st)], f"DOFull{st}")
         loaded += 1
+    if loaded:
+        yield load_drow(0, 0)
+        yield load_drow(1, 0)
     i = 0
     while i < loaded:
         st = i & 1
         yield ("delay", sim.d(1, 300))
+        if "drow_no_wait" in mut and i + 1 < loaded:
+            yield load_drow(0, i + 1)
+            yield load_drow(1, i + 1)
         if not (yield ("wait",) + stage_bar("DrainQ", i, mut)):
             break
+        # the D row half of tile i+1 once the warps that read it for tile i have drained
+        if i + 1 < loaded and "drow_no_wait" not in mut:
+            yield load_drow(0, i + 1)
         if "stage_q_half" in mut:
             yield ("reduce", [(("Q", st), f"stage{i}")])
         else:
             yield ("reduce", DS_all(f"stage{i}"))
         if not (yield ("wait",) + stage_bar("DrainDO", i, mut)):
             break
+        if i + 1 < loaded and "drow_no_wait" not in mut:
+            yield load_drow(1, i + 1)
         yield ("reduce", DO_all(st, f"stage{i}"))
         yield ("wait_read", 1)
         if "dpfull_no_producer" not in mut:
@@ -92,7 +111,7 @@ def producer(sim, n, mut):
             if not (yield ("wait",) + stage_bar("KDone", i, mut)):
                 break
         if nxt:
-            yield ("load", [(("Q", st), f"Q{i + 2}")], f"QFull{st}")
+            yield ("load", [(("Q", st), f"Q{i + 2}"), (("LSE", st), f"L{i + 2}")], f"QFull{st}")
         yield ("wait_read", 0)
         if nxt:
             yield ("load", [(res, f"DO{i + 2}") for res, _ in DO_all(st)], f"DOFull{st}")
@@ -106,6 +125,9 @@ def producer(sim, n, mut):
             ii = loaded - back
             yield ("wait", f"QFull{ii & 1}", ii >> 1)
             yield ("wait", f"DOFull{ii & 1}", ii >> 1)
+    for half in (0, 1):
+        if drows[half]:
+            yield ("wait", f"DRow{half}", drows[half] - 1)
 
 
 def mma(sim, n, mut):
@@ -165,17 +187,24 @@ def softmax(sim, n, h, q, mut):
     for i in range(n):
         st = i & 1
         yield ("delay", sim.d(1, 300))
+        ok = yield ("wait", f"QFull{st}", i >> 1)  # the LSE row, loaded with the Q tile
+        if not ok:
+            break
         ok = yield ("wait", "SFull", i)
         if not ok:
             break
-        yield ("access", [(("S", h, "P", q), "R", f"S{i}"), (("S", h, "dS", q), "R", f"S{i}")], sim.d(200, 700))
+        yield ("access", [(("S", h, "P", q), "R", f"S{i}"), (("S", h, "dS", q), "R", f"S{i}"),
+                          (("LSE", st), "R", f"L{i}")], sim.d(200, 700))
         yield ("delay", sim.d(300, 1200))  # probabilities
         yield ("access", [(("S", h, "P", q), "W", f"P{i}")], sim.d(50, 300))
         yield ("arrive", "PReady")
+        ok = yield ("wait", f"DRow{h}", i)  # this half of the D row
+        if not ok:
+            break
         ok = yield ("wait", "DPFull", i)
         if not ok:
             break
-        yield ("access", [(("DP", h, q), "R", f"dP{i}")], sim.d(100, 400))
+        yield ("access", [(("DP", h, q), "R", f"dP{i}"), (("D", h), "R", f"D{i}")], sim.d(100, 400))
         yield ("delay", sim.d(100, 600))
         yield ("access", [(("S", h, "dS", q), "W", f"dS{i}"), (("DS", h, q), "W", f"dSs{i}")], sim.d(50, 300))
         yield ("arrive", "DSReady")
@@ -219,6 +248,8 @@ def simulate(seed, n, mut=(), jitter=0.05, fault=None, keep=False):
     sim.barrier("DQEmpty", 8)
     sim.barrier("Final")
     sim.barrier("EpiDone", 8)
+    sim.barrier("DRow0")
+    sim.barrier("DRow1")
     sim.spawn("producer", producer(sim, n, mut))
     sim.spawn("mma", mma(sim, n, mut))
     for w in range(8):
@@ -239,7 +270,7 @@ def test_empty_walk():
 
 
 @pytest.mark.parametrize("mutation", ["kdone_single", "stage_q_half", "dpfull_no_producer", "no_dqempty_wait",
-                                      "no_kdone_wait", "no_epidone_wait"])
+                                      "no_kdone_wait", "no_epidone_wait", "drow_no_wait"])
 def test_planted_protocol_mistake_is_caught(mutation):
     caught = [s for s in range(400) if simulate(s, 2 + s % 6, (mutation,), jitter=0.1)]
     assert caught, f"{mutation} passed every timing"
