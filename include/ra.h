@@ -249,7 +249,9 @@ size_t ra_backward_workspace_bytes(int64_t B, int64_t H, int64_t S, int64_t D);
  *   D_i = dO_i.O_i;  P_ij = exp(s_ij - LSE_i);  dS_ij = P_ij (dO_i.V_j - D_i);
  *   dV_j = sum_i P_ij dO_i;  dQ_i = scale sum_j dS_ij K_j;  dK_j = scale sum_i dS_ij Q_i.
  *   q, k, v, o, dout: device [B,H,S,D] `dtype`, shard-major; lse: device fp32
- *   [B,H,S] from ra_forward with the same arguments.
+ *   [B,H,S] from ra_forward with the same arguments.  The tensor-core kernel (see
+ *   ra_backward_path) reads LSE rows 16 bytes at a time: an LSE that is only
+ *   4-byte aligned is accepted, and such a call runs the CUDA-core kernel.
  *   dq, dk, dv: device [B,H,S,D] `dtype`, shard-major (written).
  *   workspace: device, >= ra_backward_workspace_bytes(B,H,S,D) bytes, 256-byte
  *   aligned, caller-owned; its contents on entry do not matter.
